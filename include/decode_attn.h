@@ -1,0 +1,167 @@
+/*
+ * decode_attn.h - C ABI of the paged grouped-query decode attention library
+ * (libpaged_gqa_decode.so, CUDA kernels for sm_103a).
+ *
+ * The operation (one decode step, one query token per sequence):
+ *   for every batch entry b and query head hq, with KV head h = hq / G,
+ *   G = Hq / Hkv, L = seq_lens[b] and lo = (window > 0) ? max(0, L - window) : 0,
+ *     out[b][hq][:] = sum_{t in [lo, L)} softmax_t(scale * q[b][hq] . k_t) * v_t
+ *   where k_t = k_pages[page_table[b][t / PS]][t % PS][h][:] (likewise v_t).
+ * Defined by: apache/tvm pull request 20426 "webgpu-decode-attention"
+ * (sharded-nest commit: paged decode attention, shards of the context with
+ * online-softmax states merged afterwards, short contexts in one pass, the
+ * nest chosen on the host; PR description: sliding windows), and
+ * BackendStack21/mlx-runner pull request 3, commit "GQA-shared split
+ * attention" (one K/V row read serves every query head of its GQA group;
+ * split partials merged in a fixed order by a combine kernel).
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   q           [B][Hq][D]              fp16
+ *   k_pages     [P][PS][Hkv][D]         fp16   (the caller's paged cache)
+ *   v_pages     [P][PS][Hkv][D]         fp16
+ *   page_table  [B][max_pages_per_seq]  int32  (physical page of each logical page)
+ *   seq_lens    [B]                     int32  (positions to attend, the new
+ *                                                token's K/V already in the cache)
+ *   out         [B][Hq][D]              fp16
+ * Ownership: the caller owns every buffer, including the workspace; the
+ * library allocates no device memory and keeps no per-call state (only a
+ * per-device cache of the SM count).  Entry points are thread-safe.
+ * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ * default stream); nothing synchronises the host.
+ * Errors: a negative return means nothing was launched (bad argument) or a
+ * CUDA runtime error was reported while launching; decode_attn_strerror()
+ * names it.  Problems only the device can see (a page id outside [0, P) in
+ * an attended range, a length outside [0, max_pages_per_seq * PS] or above
+ * max_seq_len) are OR-ed as DECODE_ATTN_DEV_* bits into *err_flag (when
+ * err_flag is not NULL) and the affected output rows are written as zeros;
+ * the kernels never trap.
+ */
+#ifndef PAGED_GQA_DECODE_ATTN_H
+#define PAGED_GQA_DECODE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DECODE_ATTN_OK 0
+#define DECODE_ATTN_ERR_NULL (-1)       /* a required pointer is NULL */
+#define DECODE_ATTN_ERR_SHAPE (-2)      /* non-positive size, Hq % Hkv != 0, ... */
+#define DECODE_ATTN_ERR_HEAD_DIM (-3)   /* head_dim not in {64, 128, 256} */
+#define DECODE_ATTN_ERR_PAGE_SIZE (-4)  /* page_size not a power of two in [8, 256] */
+#define DECODE_ATTN_ERR_GROUP (-5)      /* G = Hq / Hkv above 16 */
+#define DECODE_ATTN_ERR_WORKSPACE (-6)  /* workspace missing or smaller than required */
+#define DECODE_ATTN_ERR_ALIGN (-7)      /* a tensor pointer is not 16-byte aligned */
+#define DECODE_ATTN_ERR_CUDA (-8)       /* CUDA runtime error (device query or launch) */
+#define DECODE_ATTN_ERR_TENSOR_MAP (-9) /* the TMA descriptor for the K/V pool was rejected */
+#define DECODE_ATTN_ERR_VARIANT (-10)   /* requested kernel variant cannot run this shape */
+
+/* Device error bits OR-ed into *err_flag. */
+#define DECODE_ATTN_DEV_BAD_LEN 1       /* seq_len < 0 or > max_pages_per_seq * page_size */
+#define DECODE_ATTN_DEV_BAD_PAGE 2      /* page id outside [0, num_pages) in an attended range */
+#define DECODE_ATTN_DEV_OVER_HINT 4     /* seq_len beyond the max_seq_len the grid was planned for */
+#define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed */
+
+/* Kernel variants (decode_attn_params.variant). */
+#define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
+#define DECODE_ATTN_VARIANT_SIMT 1      /* CUDA-core q.k / p.v with warp-shuffle reductions */
+#define DECODE_ATTN_VARIANT_MMA 2       /* tensor-core mma.sync q.k / p.v */
+
+typedef struct decode_attn_params {
+  int32_t batch;             /* B >= 0 */
+  int32_t num_q_heads;       /* Hq > 0 */
+  int32_t num_kv_heads;      /* Hkv > 0, Hq % Hkv == 0, G = Hq / Hkv <= 16 */
+  int32_t head_dim;          /* D in {64, 128, 256} */
+  int32_t page_size;         /* PS: power of two in [8, 256] */
+  int32_t max_pages_per_seq; /* columns of page_table (> 0) */
+  int32_t num_pages;         /* P: pages in k_pages / v_pages (> 0) */
+  int32_t max_seq_len;       /* host-known bound on seq_lens, sizes the grid;
+                                <= 0 means max_pages_per_seq * page_size */
+  float scale;               /* multiplies q . k before the softmax */
+  int32_t window;            /* <= 0: whole context; else the last min(L, window) positions */
+  int32_t variant;           /* DECODE_ATTN_VARIANT_*; 0 = automatic */
+  int32_t split_min;         /* contexts above this use shards + combine; <= 0 means 256 */
+  int32_t force_chunk;       /* > 0: tokens per shard (rounded up to 64); 0 = planner */
+} decode_attn_params;
+
+/* Launch plan chosen by the host heuristic (exposed for inspection/tests). */
+typedef struct decode_attn_plan {
+  int32_t split;             /* 0: single pass writes out; 1: shards + combine */
+  int32_t variant;           /* DECODE_ATTN_VARIANT_SIMT or _MMA */
+  int32_t group_pad;         /* G rounded up to the kernel's head group (1,2,4,8,16) */
+  int32_t tile_tokens;       /* tokens per pipeline stage (64) */
+  int32_t chunk_tokens;      /* C: tokens per shard, a multiple of tile_tokens */
+  int32_t max_shards;        /* S_max: shards of the longest planned sequence */
+  int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (shard, kv head, batch) */
+  int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
+  size_t workspace_bytes;    /* partials: B*Hq*S_max*(D+2)*4 rounded; 0 if single pass */
+} decode_attn_plan;
+
+/*
+ * Host heuristic (apache/tvm pull request 20426: the nest is picked on the
+ * host, sharded above 256 tokens; BackendStack21/mlx-runner pull request 3:
+ * split at context >= a threshold, 256 by default).  Reads only *p and
+ * num_sms; touches no device.  Returns DECODE_ATTN_OK or a negative code.
+ */
+int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sms, decode_attn_plan* plan);
+
+/* Workspace bytes decode_attn needs for *p on `device` (queries its SM
+ * count once).  Returns 0 for a single-pass plan or an invalid *p. */
+size_t decode_attn_workspace_size(const decode_attn_params* p, int device);
+
+/*
+ * One decode step: plan, split kernel, and (when split) the ordered combine,
+ * enqueued on `stream`.  workspace: device memory of at least
+ * decode_attn_workspace_size() bytes, 256-byte aligned, owned by the caller;
+ * its contents need no initialisation and are scratch after the call.
+ * err_flag: nullable device int32, bits DECODE_ATTN_DEV_* are OR-ed in (the
+ * caller clears it).  All tensor pointers must be 16-byte aligned.
+ */
+int decode_attn(const decode_attn_params* p, const void* q, const void* k_pages,
+                const void* v_pages, const int32_t* page_table, const int32_t* seq_lens,
+                void* out, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                void* stream);
+
+/*
+ * The two launches decode_attn makes, callable separately (e.g. to time the
+ * split kernel alone).  decode_attn_split runs the shard kernel (and, for a
+ * single-pass plan, writes out); decode_attn_combine merges the partials in
+ * ascending shard order and is a no-op returning DECODE_ATTN_OK for a
+ * single-pass plan.  Arguments as for decode_attn; the plan is recomputed
+ * from *p and must be the same for both calls.
+ */
+int decode_attn_split(const decode_attn_params* p, const void* q, const void* k_pages,
+                      const void* v_pages, const int32_t* page_table, const int32_t* seq_lens,
+                      void* out, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                      void* stream);
+int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, void* out,
+                        void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                        void* stream);
+
+/*
+ * End-to-end step from HOST buffers: enqueues the host-to-device copies of
+ * q, k_pages, v_pages, page_table and seq_lens into the caller's device
+ * buffers (d_* arguments, same layouts), decode_attn, and the device-to-host
+ * copy of out into out_host.  Host buffers should be pinned for the copies to
+ * be asynchronous.  Nothing synchronises: the caller waits on `stream`
+ * before reading out_host.  kv_bytes_to_copy: bytes of each of k_pages and
+ * v_pages to copy (the pool prefix in use); 0 copies the whole pool.
+ */
+int decode_attn_host(const decode_attn_params* p, const void* q_host, const void* k_pages_host,
+                     const void* v_pages_host, const int32_t* page_table_host,
+                     const int32_t* seq_lens_host, void* out_host, void* d_q, void* d_k_pages,
+                     void* d_v_pages, int32_t* d_page_table, int32_t* d_seq_lens, void* d_out,
+                     size_t kv_bytes_to_copy, void* workspace, size_t workspace_bytes,
+                     int32_t* err_flag, void* stream);
+
+/* Static text for a return code. */
+const char* decode_attn_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_GQA_DECODE_ATTN_H */

@@ -1,0 +1,264 @@
+"""Paged grouped-query decode attention for GB300 (sm_103a).
+
+Thin binding over the C ABI in ``include/decode_attn.h`` (the shared library
+``_build/libpaged_gqa_decode.so``, built by ``build.build()``).  This module
+only marshals arguments: torch tensors become raw device pointers, the
+current CUDA stream becomes the ``stream`` argument, and the workspace is a
+torch allocation cached per device.  Every step of the computation runs in
+the library's CUDA kernels; there is no other code path, and calling any
+entry point without the built library raises.
+
+Entry points (same names as the C ABI):
+  decode_attn, decode_attn_split, decode_attn_combine, decode_attn_host,
+  decode_attn_workspace_size, decode_attn_make_plan, decode_attn_strerror
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "DecodeAttnParams", "DecodeAttnPlan", "DecodeAttnError", "load_library", "library_path",
+    "make_params", "decode_attn", "decode_attn_split", "decode_attn_combine",
+    "decode_attn_host", "decode_attn_workspace_size", "decode_attn_make_plan",
+    "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
+    "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
+]
+
+VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
+DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT = 1, 2, 4, 8
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", "libpaged_gqa_decode.so")
+
+
+class DecodeAttnParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
+        "max_pages_per_seq", "num_pages", "max_seq_len")] + [
+        ("scale", ctypes.c_float), ("window", ctypes.c_int32), ("variant", ctypes.c_int32),
+        ("split_min", ctypes.c_int32), ("force_chunk", ctypes.c_int32)]
+
+
+class DecodeAttnPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "split", "variant", "group_pad", "tile_tokens", "chunk_tokens", "max_shards",
+        "grid_x", "grid_y", "grid_z", "ctas_per_sm")] + [("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class DecodeAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {decode_attn_strerror(code)} (status {code})")
+        self.code = code
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library():
+    """The CUDA library, loaded once.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library not built ({path} missing); run "
+                    "paged_gqa_decode_06_gb300.build.build()")
+            lib = ctypes.CDLL(path)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            PP = ctypes.POINTER(DecodeAttnParams)
+            lib.decode_attn_make_plan.argtypes = [PP, i32, ctypes.POINTER(DecodeAttnPlan)]
+            lib.decode_attn_make_plan.restype = ctypes.c_int
+            lib.decode_attn_workspace_size.argtypes = [PP, ctypes.c_int]
+            lib.decode_attn_workspace_size.restype = sz
+            for name in ("decode_attn", "decode_attn_split"):
+                f = getattr(lib, name)
+                f.argtypes = [PP, P, P, P, P, P, P, P, sz, P, P]
+                f.restype = ctypes.c_int
+            lib.decode_attn_combine.argtypes = [PP, P, P, P, sz, P, P]
+            lib.decode_attn_combine.restype = ctypes.c_int
+            lib.decode_attn_host.argtypes = [PP] + [P] * 13 + [sz, P, sz, P, P]
+            lib.decode_attn_host.restype = ctypes.c_int
+            lib.decode_attn_strerror.argtypes = [ctypes.c_int]
+            lib.decode_attn_strerror.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def decode_attn_strerror(code: int) -> str:
+    return load_library().decode_attn_strerror(int(code)).decode()
+
+
+def make_params(q, k_pages, page_table, scale: float, window: int = 0,
+                max_seq_len: Optional[int] = None, variant: int = VARIANT_AUTO,
+                split_min: int = 0, force_chunk: int = 0) -> DecodeAttnParams:
+    """Parameters from tensor shapes: q [B,Hq,D], k_pages [P,PS,Hkv,D],
+    page_table [B,maxPages].  ``max_seq_len`` is a host-side bound on
+    seq_lens (it sizes the grid; None = the page table's capacity)."""
+    B, Hq, D = q.shape
+    P, PS, Hkv, D2 = k_pages.shape
+    if D2 != D:
+        raise ValueError("q and k_pages head_dim differ")
+    return DecodeAttnParams(
+        batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=PS,
+        max_pages_per_seq=page_table.shape[1], num_pages=P,
+        max_seq_len=int(max_seq_len) if max_seq_len else 0, scale=float(scale),
+        window=int(window), variant=int(variant), split_min=int(split_min),
+        force_chunk=int(force_chunk))
+
+
+def decode_attn_make_plan(params: DecodeAttnParams, num_sms: int) -> DecodeAttnPlan:
+    plan = DecodeAttnPlan()
+    st = load_library().decode_attn_make_plan(ctypes.byref(params), int(num_sms),
+                                              ctypes.byref(plan))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_make_plan")
+    return plan
+
+
+def decode_attn_workspace_size(params: DecodeAttnParams, device: int) -> int:
+    return int(load_library().decode_attn_workspace_size(ctypes.byref(params), int(device)))
+
+
+# ------------------------------------------------------------ torch glue
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes: int):
+    import torch
+    if nbytes == 0:
+        return None
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, dtype, name, device=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_seq_len,
+             variant, split_min, force_chunk, workspace):
+    import torch
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_attn runs on CUDA tensors (use decode_attn_host for host "
+                         "buffers)")
+    _check(q, torch.float16, "q", dev)
+    _check(k_pages, torch.float16, "k_pages", dev)
+    _check(v_pages, torch.float16, "v_pages", dev)
+    _check(page_table, torch.int32, "page_table", dev)
+    _check(seq_lens, torch.int32, "seq_lens", dev)
+    if v_pages.shape != k_pages.shape:
+        raise ValueError("k_pages and v_pages shapes differ")
+    p = make_params(q, k_pages, page_table, scale, window, max_seq_len, variant, split_min,
+                    force_chunk)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, torch.float16, "out", dev)
+    need = decode_attn_workspace_size(p, dev.index if dev.index is not None else
+                                      torch.cuda.current_device())
+    if workspace is None:
+        workspace = _workspace(dev, need)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return p, out, workspace, ws_bytes
+
+
+def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
+                out=None, max_seq_len: Optional[int] = None, workspace=None, err_flag=None,
+                variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
+                stream=None):
+    """One decode step of paged GQA attention; returns ``out`` [B,Hq,D] fp16.
+
+    q [B,Hq,D] fp16, k_pages/v_pages [P,PS,Hkv,D] fp16, page_table [B,maxPages]
+    int32, seq_lens [B] int32, all on one CUDA device.  ``window`` > 0 attends
+    the last min(L, window) positions.  ``err_flag``: optional int32 device
+    tensor of one element that receives DEV_* bits.  Enqueued on ``stream``
+    (default: torch's current stream); does not synchronise."""
+    p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
+                                    window, max_seq_len, variant, split_min, force_chunk,
+                                    workspace)
+    st = load_library().decode_attn(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                                    _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(ws),
+                                    ws_bytes, _ptr(err_flag), _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn")
+    return out
+
+
+def decode_attn_split(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
+                      out=None, max_seq_len=None, workspace=None, err_flag=None,
+                      variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
+                      stream=None):
+    """The shard kernel alone (writes ``out`` directly for a single-pass plan,
+    partials into ``workspace`` otherwise).  Returns (out, workspace)."""
+    p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
+                                    window, max_seq_len, variant, split_min, force_chunk,
+                                    workspace)
+    st = load_library().decode_attn_split(ctypes.byref(p), _ptr(q), _ptr(k_pages),
+                                          _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
+                                          _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
+                                          _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_split")
+    return out, ws
+
+
+def decode_attn_combine(params: DecodeAttnParams, seq_lens, out, workspace, err_flag=None,
+                        stream=None):
+    """The ordered combine alone, for ``params`` as used by decode_attn_split."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().decode_attn_combine(ctypes.byref(params), _ptr(seq_lens), _ptr(out),
+                                            _ptr(workspace), ws_bytes, _ptr(err_flag),
+                                            _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_combine")
+    return out
+
+
+def decode_attn_host(params: DecodeAttnParams, q_host, k_host, v_host, table_host, lens_host,
+                     out_host, d_q, d_k, d_v, d_table, d_lens, d_out, workspace,
+                     kv_bytes_to_copy: int = 0, err_flag=None, stream=None):
+    """End-to-end step from host buffers (pinned CPU tensors): copies in,
+    decode_attn, copies ``out`` back; enqueued on ``stream``, not awaited."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load_library().decode_attn_host(
+        ctypes.byref(params), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(table_host),
+        _ptr(lens_host), _ptr(out_host), _ptr(d_q), _ptr(d_k), _ptr(d_v), _ptr(d_table),
+        _ptr(d_lens), _ptr(d_out), int(kv_bytes_to_copy), _ptr(workspace), ws_bytes,
+        _ptr(err_flag), _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_host")
+    return out_host

@@ -1,0 +1,409 @@
+// C ABI of the decode-attention library: argument checks, the host planner,
+// TMA descriptors for the paged K/V pool, and the launches.
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+
+using namespace pgd;
+
+namespace {
+
+constexpr int kDefaultSplitMin = 256;
+constexpr int kMaxDevices = 64;
+// Planner cost of one CTA beyond its tokens (launch, page ids, first TMA
+// round trip, partial write), in tokens of streaming.
+constexpr int kCtaOverheadTokens = 64;
+constexpr int kSmemPerSm = 228 * 1024;
+
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count(int device, int* out) {
+  if (device < 0 || device >= kMaxDevices) return DECODE_ATTN_ERR_CUDA;
+  int n = g_sm_count[device].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        n <= 0)
+      return DECODE_ATTN_ERR_CUDA;
+    g_sm_count[device].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return DECODE_ATTN_OK;
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+int check_params(const decode_attn_params* p) {
+  if (!p) return DECODE_ATTN_ERR_NULL;
+  if (p->batch < 0 || p->batch > 65535 || p->num_q_heads <= 0 || p->num_kv_heads <= 0 ||
+      p->num_kv_heads > 65535 || p->num_q_heads % p->num_kv_heads != 0 ||
+      p->max_pages_per_seq <= 0 || p->num_pages <= 0)
+    return DECODE_ATTN_ERR_SHAPE;
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
+    return DECODE_ATTN_ERR_HEAD_DIM;
+  if (!is_pow2(p->page_size) || p->page_size < 8 || p->page_size > 256)
+    return DECODE_ATTN_ERR_PAGE_SIZE;
+  if ((int64_t)p->max_pages_per_seq * p->page_size > INT32_MAX / 2 ||
+      (int64_t)p->num_pages * p->page_size >= INT32_MAX)
+    return DECODE_ATTN_ERR_SHAPE;
+  if (p->num_q_heads / p->num_kv_heads > 16) return DECODE_ATTN_ERR_GROUP;
+  if (!std::isfinite(p->scale)) return DECODE_ATTN_ERR_SHAPE;
+  return DECODE_ATTN_OK;
+}
+
+int next_pow2(int x) {
+  int r = 1;
+  while (r < x) r <<= 1;
+  return r;
+}
+
+}  // namespace
+
+namespace pgd {
+size_t simt_smem_bytes(int head_dim) {
+  switch (head_dim) {
+    case 64: return SimtCfg<64>::kSmemBytes;
+    case 128: return SimtCfg<128>::kSmemBytes;
+    default: return SimtCfg<256>::kSmemBytes;
+  }
+}
+int simt_ctas_per_sm(int head_dim) {
+  // dynamic ring + static smem (page coordinates, barriers, scratch) + 1 KB
+  const size_t per_cta = simt_smem_bytes(head_dim) + kMaxPieces * 4 + 2048 + 1024;
+  return std::max<int>(1, (int)(kSmemPerSm / per_cta));
+}
+}  // namespace pgd
+
+extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sms,
+                                     decode_attn_plan* plan) {
+  int st = check_params(p);
+  if (st) return st;
+  if (!plan) return DECODE_ATTN_ERR_NULL;
+  if (num_sms <= 0) return DECODE_ATTN_ERR_SHAPE;
+  std::memset(plan, 0, sizeof(*plan));
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const int gp = next_pow2(G);
+  int variant = p->variant;
+  if (variant == DECODE_ATTN_VARIANT_AUTO) variant = DECODE_ATTN_VARIANT_SIMT;
+  if (variant != DECODE_ATTN_VARIANT_SIMT) return DECODE_ATTN_ERR_VARIANT;
+  if (gp > 8) return DECODE_ATTN_ERR_VARIANT;
+
+  const int64_t capacity = (int64_t)p->max_pages_per_seq * p->page_size;
+  const int64_t max_len =
+      p->max_seq_len > 0 ? std::min<int64_t>(p->max_seq_len, capacity) : capacity;
+  const int64_t attended = p->window > 0 ? std::min<int64_t>(max_len, p->window) : max_len;
+  // positions from the tile-aligned base to the end of the longest sequence
+  const int64_t span = std::max<int64_t>(1, p->window > 0 ? attended + kTile - 1 : max_len);
+  const int box_t = std::min(p->page_size, kTile);
+  const int64_t max_chunk = (int64_t)kMaxPieces * box_t;
+  const int split_min = p->split_min > 0 ? p->split_min : kDefaultSplitMin;
+  const int ctas_per_sm = simt_ctas_per_sm(p->head_dim);
+
+  int64_t chunk;
+  if (p->force_chunk > 0) {
+    chunk = round_up(p->force_chunk, kTile);
+    if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
+  } else if (attended <= split_min) {
+    chunk = round_up(span, kTile);  // one shard covers the whole range
+  } else {
+    // choose the shard count minimising (waves of CTAs) x (tokens per CTA +
+    // fixed cost): CTAs = units * S, all of equal length for the longest
+    // sequence; ties go to fewer shards (fewer partials to merge)
+    const int64_t units = std::max<int64_t>(1, (int64_t)p->batch * p->num_kv_heads);
+    const int64_t slots = (int64_t)num_sms * ctas_per_sm;
+    const int64_t s_hi = std::max<int64_t>(1, ceil_div(span, kTile));
+    int64_t best_cost = INT64_MAX;
+    chunk = round_up(span, kTile);
+    for (int64_t S = 1; S <= s_hi; ++S) {
+      const int64_t c = round_up(ceil_div(span, S), kTile);
+      if (c > max_chunk) continue;
+      const int64_t s_eff = ceil_div(span, c);
+      if (s_eff != S) continue;  // same chunk as a smaller S
+      const int64_t waves = ceil_div(units * s_eff, slots);
+      const int64_t cost = waves * (c + kCtaOverheadTokens);
+      if (cost < best_cost) {
+        best_cost = cost;
+        chunk = c;
+      }
+    }
+  }
+  if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
+  const int64_t max_shards = ceil_div(span, chunk);
+  if (max_shards > 65535) return DECODE_ATTN_ERR_SHAPE;
+
+  plan->variant = variant;
+  plan->group_pad = gp;
+  plan->tile_tokens = kTile;
+  plan->chunk_tokens = (int32_t)chunk;
+  plan->max_shards = (int32_t)max_shards;
+  plan->split = max_shards > 1 ? 1 : 0;
+  plan->grid_x = (int32_t)max_shards;
+  plan->grid_y = p->num_kv_heads;
+  plan->grid_z = p->batch;
+  plan->ctas_per_sm = ctas_per_sm;
+  if (plan->split) {
+    const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)max_shards;
+    plan->workspace_bytes = round_up(rows * sizeof(float2), 256) + rows * p->head_dim * 4;
+  }
+  return DECODE_ATTN_OK;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D view of a [P][PS][Hkv][D] fp16 pool: (d, kv head, P*PS token rows);
+// one box = box_t consecutive rows of one KV head.
+int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params* p, int box_t) {
+  auto fn = encode_fn();
+  if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
+  const int D = p->head_dim;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p->num_kv_heads,
+                        (cuuint64_t)p->num_pages * p->page_size};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p->num_kv_heads * D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_t};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+int plan_for_stream(const decode_attn_params* p, cudaStream_t stream, decode_attn_plan* plan) {
+  (void)stream;
+  int st = check_params(p);  // argument errors are reported before any CUDA call
+  if (st) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DECODE_ATTN_ERR_CUDA;
+  int n = 0;
+  st = sm_count(dev, &n);
+  if (st) return st;
+  return decode_attn_make_plan(p, n, plan);
+}
+
+struct Workspace {
+  float2* ml;
+  float* acc;
+};
+
+int workspace_views(const decode_attn_params* p, const decode_attn_plan& plan, void* ws,
+                    size_t ws_bytes, Workspace* out) {
+  out->ml = nullptr;
+  out->acc = nullptr;
+  if (!plan.split) return DECODE_ATTN_OK;
+  if (!ws || ws_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
+    return DECODE_ATTN_ERR_WORKSPACE;
+  const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)plan.max_shards;
+  out->ml = reinterpret_cast<float2*>(ws);
+  out->acc = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                      round_up(rows * sizeof(float2), 256));
+  return DECODE_ATTN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DECODE_ATTN_OK : DECODE_ATTN_ERR_CUDA; }
+
+int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const void* q,
+              const void* k_pages, const void* v_pages, const int32_t* page_table,
+              const int32_t* seq_lens, void* out, const Workspace& ws, int32_t* err_flag,
+              cudaStream_t stream) {
+  if (p->batch == 0) return DECODE_ATTN_OK;
+  SplitLaunch L;
+  const int box_t = std::min(p->page_size, kTile);
+  int st = encode_pool_map(&L.tmap_k, k_pages, p, box_t);
+  if (!st) st = encode_pool_map(&L.tmap_v, v_pages, p, box_t);
+  if (st) return st;
+  SplitArgs& a = L.args;
+  a.q = static_cast<const __half*>(q);
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.out = static_cast<__half*>(out);
+  a.ws_acc = ws.acc;
+  a.ws_ml = ws.ml;
+  a.err = err_flag;
+  a.Hq = p->num_q_heads;
+  a.Hkv = p->num_kv_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
+  a.max_pages = p->max_pages_per_seq;
+  a.num_pages = p->num_pages;
+  a.page_size = p->page_size;
+  a.page_shift = ilog2(p->page_size);
+  a.box_tokens = box_t;
+  a.window = p->window > 0 ? p->window : 0;
+  a.chunk = plan.chunk_tokens;
+  a.max_shards = plan.max_shards;
+  a.split = plan.split;
+  a.scale_log2 = p->scale * kLog2e;
+  L.grid = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
+  L.group_pad = plan.group_pad;
+  L.variant = plan.variant;
+  L.stream = stream;
+  switch (p->head_dim) {
+    case 64: return cuda_status(launch_split_d64(L));
+    case 128: return cuda_status(launch_split_d128(L));
+    default: return cuda_status(launch_split_d256(L));
+  }
+}
+
+int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
+                const int32_t* seq_lens, void* out, const Workspace& ws, cudaStream_t stream) {
+  if (!plan.split || p->batch == 0) return DECODE_ATTN_OK;
+  CombineArgs a;
+  a.seq_lens = seq_lens;
+  a.ws_acc = ws.acc;
+  a.ws_ml = ws.ml;
+  a.out = static_cast<__half*>(out);
+  a.B = p->batch;
+  a.Hq = p->num_q_heads;
+  a.capacity = p->max_pages_per_seq * p->page_size;
+  a.window = p->window > 0 ? p->window : 0;
+  a.chunk = plan.chunk_tokens;
+  a.max_shards = plan.max_shards;
+  switch (p->head_dim) {
+    case 64: return cuda_status(launch_combine_d64(a, stream));
+    case 128: return cuda_status(launch_combine_d128(a, stream));
+    default: return cuda_status(launch_combine_d256(a, stream));
+  }
+}
+
+int check_tensors(const void* q, const void* k_pages, const void* v_pages,
+                  const int32_t* page_table, const int32_t* seq_lens, const void* out) {
+  if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out) return DECODE_ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return DECODE_ATTN_ERR_ALIGN;
+  return DECODE_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" size_t decode_attn_workspace_size(const decode_attn_params* p, int device) {
+  int n = 0;
+  if (sm_count(device, &n)) return 0;
+  decode_attn_plan plan;
+  if (decode_attn_make_plan(p, n, &plan)) return 0;
+  return plan.workspace_bytes;
+}
+
+extern "C" int decode_attn_split(const decode_attn_params* p, const void* q, const void* k_pages,
+                                 const void* v_pages, const int32_t* page_table,
+                                 const int32_t* seq_lens, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  decode_attn_plan plan;
+  int st = plan_for_stream(p, s, &plan);
+  if (st) return st;
+  if ((st = check_tensors(q, k_pages, v_pages, page_table, seq_lens, out))) return st;
+  Workspace ws;
+  if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
+  return run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s);
+}
+
+extern "C" int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   int32_t* err_flag, void* stream) {
+  (void)err_flag;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  decode_attn_plan plan;
+  int st = plan_for_stream(p, s, &plan);
+  if (st) return st;
+  if (!seq_lens || !out) return DECODE_ATTN_ERR_NULL;
+  if (!aligned16(out)) return DECODE_ATTN_ERR_ALIGN;
+  Workspace ws;
+  if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
+  return run_combine(p, plan, seq_lens, out, ws, s);
+}
+
+extern "C" int decode_attn(const decode_attn_params* p, const void* q, const void* k_pages,
+                           const void* v_pages, const int32_t* page_table,
+                           const int32_t* seq_lens, void* out, void* workspace,
+                           size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  decode_attn_plan plan;
+  int st = plan_for_stream(p, s, &plan);
+  if (st) return st;
+  if ((st = check_tensors(q, k_pages, v_pages, page_table, seq_lens, out))) return st;
+  Workspace ws;
+  if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
+  st = run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s);
+  if (st) return st;
+  return run_combine(p, plan, seq_lens, out, ws, s);
+}
+
+extern "C" int decode_attn_host(const decode_attn_params* p, const void* q_host,
+                                const void* k_pages_host, const void* v_pages_host,
+                                const int32_t* page_table_host, const int32_t* seq_lens_host,
+                                void* out_host, void* d_q, void* d_k_pages, void* d_v_pages,
+                                int32_t* d_page_table, int32_t* d_seq_lens, void* d_out,
+                                size_t kv_bytes_to_copy, void* workspace,
+                                size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  int st = check_params(p);
+  if (st) return st;
+  if (!q_host || !k_pages_host || !v_pages_host || !page_table_host || !seq_lens_host ||
+      !out_host)
+    return DECODE_ATTN_ERR_NULL;
+  if ((st = check_tensors(d_q, d_k_pages, d_v_pages, d_page_table, d_seq_lens, d_out))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t D = p->head_dim;
+  const size_t q_bytes = (size_t)p->batch * p->num_q_heads * D * 2;
+  const size_t pool = (size_t)p->num_pages * p->page_size * p->num_kv_heads * D * 2;
+  const size_t kv = (kv_bytes_to_copy == 0 || kv_bytes_to_copy > pool) ? pool : kv_bytes_to_copy;
+  const size_t pt_bytes = (size_t)p->batch * p->max_pages_per_seq * 4;
+  const size_t sl_bytes = (size_t)p->batch * 4;
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_q, q_host, q_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_k_pages, k_pages_host, kv, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_v_pages, v_pages_host, kv, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_page_table, page_table_host, pt_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_seq_lens, seq_lens_host, sl_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return DECODE_ATTN_ERR_CUDA;
+  st = decode_attn(p, d_q, d_k_pages, d_v_pages, d_page_table, d_seq_lens, d_out, workspace,
+                   workspace_bytes, err_flag, stream);
+  if (st) return st;
+  e = cudaMemcpyAsync(out_host, d_out, q_bytes, cudaMemcpyDeviceToHost, s);
+  return cuda_status(e);
+}
+
+extern "C" const char* decode_attn_strerror(int status) {
+  switch (status) {
+    case DECODE_ATTN_OK: return "ok";
+    case DECODE_ATTN_ERR_NULL: return "a required pointer is NULL";
+    case DECODE_ATTN_ERR_SHAPE: return "invalid shape or size";
+    case DECODE_ATTN_ERR_HEAD_DIM: return "head_dim must be 64, 128 or 256";
+    case DECODE_ATTN_ERR_PAGE_SIZE: return "page_size must be a power of two in [8, 256]";
+    case DECODE_ATTN_ERR_GROUP: return "num_q_heads / num_kv_heads must be at most 16";
+    case DECODE_ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DECODE_ATTN_ERR_ALIGN: return "tensor pointers must be 16-byte aligned";
+    case DECODE_ATTN_ERR_CUDA: return "CUDA runtime error";
+    case DECODE_ATTN_ERR_TENSOR_MAP: return "TMA descriptor for the K/V pool rejected";
+    case DECODE_ATTN_ERR_VARIANT: return "kernel variant unavailable for this shape";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,140 @@
+// Device helpers shared by the decode-attention kernels: inline PTX for
+// mbarriers and TMA, bounded waits, and the shard arithmetic that the split
+// and combine kernels must agree on.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through cudart)
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/decode_attn.h"
+
+namespace pgd {
+
+constexpr int kTile = 64;           // tokens per pipeline stage
+constexpr int kMaxPieces = 1024;    // TMA boxes per shard (page-id table in smem)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------ PTX ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of `bar` with the given parity to complete, giving up
+// after about two seconds (returns false then).  Every spin in these kernels
+// goes through here, so a lost arrival cannot hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+
+// 3-D tiled TMA load into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, int32_t c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// 4-D tiled TMA load (used with the 128-byte swizzled view of the pool).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int32_t c0,
+                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------- shard maths ---
+
+// Attended range of one sequence and how it is cut into shards.  Shards are
+// laid on a grid of kTile-aligned absolute positions starting at `base` (the
+// window start rounded down), so every TMA box starts on a tile boundary.
+struct SeqRange {
+  int32_t start;    // first attended position
+  int32_t end;      // one past the last attended position (= seq_len)
+  int32_t base;     // start rounded down to a multiple of kTile
+  int32_t nshards;  // shards holding attended positions (0 for an empty range)
+  int32_t status;   // 0 or DECODE_ATTN_DEV_* bits
+};
+
+__device__ __forceinline__ SeqRange seq_range(int32_t L, int32_t window, int32_t capacity,
+                                              int32_t chunk, int32_t max_shards) {
+  SeqRange r{0, 0, 0, 0, 0};
+  if (L < 0 || L > capacity) {
+    r.status = DECODE_ATTN_DEV_BAD_LEN;
+    return r;
+  }
+  r.end = L;
+  r.start = (window > 0 && L > window) ? L - window : 0;
+  r.base = r.start & ~(kTile - 1);
+  r.nshards = (L > r.start) ? (L - r.base + chunk - 1) / chunk : 0;
+  if (r.nshards > max_shards) {
+    r.status = DECODE_ATTN_DEV_OVER_HINT;
+    r.nshards = 0;
+  }
+  return r;
+}
+
+__device__ __forceinline__ void raise_error(int32_t* err, int32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+}  // namespace pgd

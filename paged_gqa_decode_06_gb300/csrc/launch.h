@@ -1,0 +1,34 @@
+// Host-side interface between the C ABI (api.cu) and the per-head-dim
+// translation units that instantiate the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "combine.cuh"
+#include "split_simt.cuh"
+
+namespace pgd {
+
+struct SplitLaunch {
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  SplitArgs args;
+  dim3 grid;
+  int group_pad;
+  int variant;
+  cudaStream_t stream;
+};
+
+cudaError_t launch_split_d64(const SplitLaunch& L);
+cudaError_t launch_split_d128(const SplitLaunch& L);
+cudaError_t launch_split_d256(const SplitLaunch& L);
+cudaError_t launch_combine_d64(const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_combine_d128(const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_combine_d256(const CombineArgs& a, cudaStream_t stream);
+
+// Resident CTAs per SM the kernels are sized for (shared-memory bound).
+int simt_ctas_per_sm(int head_dim);
+size_t simt_smem_bytes(int head_dim);
+
+}  // namespace pgd

@@ -1,0 +1,158 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/*.h declares, rejects bad arguments before touching
+the device, and the planner's choices obey their contract."""
+import ctypes
+import glob
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    from paged_gqa_decode_06_gb300 import build
+    build.build()
+    import paged_gqa_decode_06_gb300 as p
+    p.load_library()
+    return p
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("#", "typedef", "return")):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("decode_attn", "decode_attn_split", "decode_attn_combine", "decode_attn_host",
+              "decode_attn_workspace_size", "decode_attn_make_plan", "decode_attn_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(pkg):
+    lib = ctypes.CDLL(pkg.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_needs_no_driver_at_load(pkg):
+    # cudart is static; the driver is only reached on the first CUDA call
+    out = os.popen(f"ldd {pkg.library_path()}").read()
+    assert "libcuda.so" not in out
+    assert "libtorch" not in out
+
+
+def params(pkg, **kw):
+    base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                max_pages_per_seq=192, num_pages=256, max_seq_len=3060, scale=0.088,
+                window=0, variant=0, split_min=0, force_chunk=0)
+    base.update(kw)
+    return pkg.DecodeAttnParams(**base)
+
+
+def test_strerror(pkg):
+    assert pkg.decode_attn_strerror(0) == "ok"
+    assert "head_dim" in pkg.decode_attn_strerror(-3)
+    assert pkg.decode_attn_strerror(-999) == "unknown status"
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, -3), ("page_size", 24, -4), ("page_size", 4, -4), ("page_size", 512, -4),
+    ("num_q_heads", 30, -2), ("num_kv_heads", 0, -2), ("batch", -1, -2),
+    ("max_pages_per_seq", 0, -2), ("num_pages", 0, -2), ("scale", float("nan"), -2),
+    ("num_q_heads", 8 * 32, -5),
+])
+def test_bad_params_rejected_before_launch(pkg, field, value, code):
+    p = params(pkg, **{field: value})
+    plan = pkg.DecodeAttnPlan()
+    lib = pkg.load_library()
+    assert lib.decode_attn_make_plan(ctypes.byref(p), 152, ctypes.byref(plan)) == code
+    # the launch entry points return the same code without any CUDA call
+    nul = None
+    assert lib.decode_attn(ctypes.byref(p), nul, nul, nul, nul, nul, nul, nul, 0, nul,
+                           nul) == code
+
+
+def test_null_params(pkg):
+    lib = pkg.load_library()
+    assert lib.decode_attn(None, None, None, None, None, None, None, None, 0, None, None) == -1
+    plan = pkg.DecodeAttnPlan()
+    assert lib.decode_attn_make_plan(None, 152, ctypes.byref(plan)) == -1
+
+
+def test_short_context_single_pass(pkg):
+    for L in (1, 64, 200, 256):
+        plan = pkg.decode_attn_make_plan(params(pkg, max_seq_len=L), 152)
+        assert plan.split == 0 and plan.max_shards == 1
+        assert plan.chunk_tokens >= L and plan.chunk_tokens % 64 == 0
+        assert plan.workspace_bytes == 0
+
+
+def test_threshold_at_256(pkg):
+    # contexts above 256 split (apache/tvm pull request 20426: "> 256")
+    plan = pkg.decode_attn_make_plan(params(pkg, max_seq_len=257), 152)
+    assert plan.split == 1 and plan.max_shards >= 2
+    plan = pkg.decode_attn_make_plan(params(pkg, max_seq_len=300, split_min=512), 152)
+    assert plan.split == 0
+
+
+def test_long_context_fills_whole_waves(pkg):
+    # B=4, Hkv=8, 131072 tokens, D=128: 32 (b, h) units on 152 SMs x 2 CTAs
+    p = params(pkg, batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
+               max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    slots = 152 * plan.ctas_per_sm
+    ctas = plan.grid_x * plan.grid_y * plan.grid_z
+    assert plan.split == 1
+    assert plan.chunk_tokens * plan.max_shards >= 131072
+    assert ctas % slots == 0 or ctas <= slots, (ctas, slots)
+    assert plan.workspace_bytes >= 4 * 64 * plan.max_shards * (128 + 2) * 4
+
+
+def test_window_plan_bounds_grid(pkg):
+    p = params(pkg, batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
+               max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072, window=4096)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    # the grid covers the window plus the tile-alignment slack, not the context
+    assert plan.chunk_tokens * plan.max_shards >= 4096 + 63
+    assert plan.chunk_tokens * (plan.max_shards - 1) < 4096 + 63
+
+
+def test_force_chunk(pkg):
+    plan = pkg.decode_attn_make_plan(params(pkg, force_chunk=100), 152)
+    assert plan.chunk_tokens == 128
+    assert plan.max_shards == math.ceil(3060 / 128)
+    with pytest.raises(pkg.DecodeAttnError):
+        pkg.decode_attn_make_plan(params(pkg, force_chunk=1 << 20), 152)
+
+
+def test_plan_is_a_pure_function(pkg):
+    a = pkg.decode_attn_make_plan(params(pkg), 152).as_dict()
+    b = pkg.decode_attn_make_plan(params(pkg), 152).as_dict()
+    assert a == b
+    c = pkg.decode_attn_make_plan(params(pkg), 76).as_dict()
+    assert c["chunk_tokens"] >= a["chunk_tokens"]
+
+
+@pytest.mark.parametrize("max_len", [257, 1000, 3060, 8192, 65536, 131072])
+@pytest.mark.parametrize("units", [(1, 8), (64, 8), (4, 8), (1, 1)])
+def test_plan_covers_every_length(pkg, max_len, units):
+    B, Hkv = units
+    PS = 16
+    p = params(pkg, batch=B, num_kv_heads=Hkv, num_q_heads=Hkv * 4,
+               max_pages_per_seq=(max_len + PS - 1) // PS, num_pages=10, max_seq_len=max_len)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    assert plan.chunk_tokens % 64 == 0
+    assert plan.chunk_tokens * plan.max_shards >= max_len
+    assert plan.chunk_tokens <= 1024 * min(PS, 64)   # page ids of one shard fit in smem
+    assert plan.grid_x == plan.max_shards and plan.grid_y == Hkv and plan.grid_z == B

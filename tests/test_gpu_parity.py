@@ -1,0 +1,332 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the f64
+oracle on the same seeded inputs.
+
+Bar (the target the method states: "0.02% relative L2 against an f64
+reference" in apache/tvm pull request 20426 is the fp16 output-rounding
+floor): relative L2 <= 5e-4 and max abs error <= 2e-3 over each config's
+fp16 outputs; per row, relative L2 <= 1e-3 to catch a localised fault.
+Integer-like facts are checked bit for bit: a one-position context returns
+the V row, relabelling pages or repeating a run changes no bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_decode_06_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+REL_L2, MAX_ABS, ROW_REL = 5e-4, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_gqa_decode_06_gb300 import build
+    build.build()
+    oracle.build()
+    import paged_gqa_decode_06_gb300 as p
+    p.load_library()
+    return p
+
+
+DEV = "cuda:0"
+
+
+def run(pkg, w, **kw):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kw.setdefault("max_seq_len", w.max_seq_len())
+    out = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                          window=kw.pop("window", w.window), err_flag=err, **kw)
+    torch.cuda.synchronize()
+    return out, int(err.item())
+
+
+def compare(got, ref, rows=None):
+    g = got.float().cpu().numpy().astype(np.float64).reshape(-1, got.shape[-1])
+    if rows is not None:
+        g = g[rows]
+    r = ref.reshape(-1, ref.shape[-1])
+    den = np.linalg.norm(r)
+    rel = np.linalg.norm(g - r) / (den if den > 0 else 1.0)
+    mab = np.abs(g - r).max() if g.size else 0.0
+    rn = np.linalg.norm(r, axis=1)
+    row_rel = np.linalg.norm(g - r, axis=1) / np.where(rn > 0, rn, 1.0)
+    return rel, mab, row_rel.max() if row_rel.size else 0.0
+
+
+def assert_parity(got, ref, rows=None, what=""):
+    rel, mab, rrel = compare(got, ref, rows)
+    assert rel <= REL_L2 and mab <= MAX_ABS and rrel <= ROW_REL, (what, rel, mab, rrel)
+    return rel, mab
+
+
+def oracle_of(w, rows=None, window=None):
+    wc = w.to("cpu")
+    return oracle.decode_attn(wc.q, wc.k_pages, wc.v_pages, wc.page_table, wc.seq_lens, wc.scale,
+                              w.window if window is None else window, rows=rows)
+
+
+# ------------------------------------------------------------- configs
+
+@pytest.mark.parametrize("name", ["tiny", "llama", "sweep_d64", "sweep_d128", "sweep_d256"])
+def test_parity_named(pkg, name):
+    w = workloads.make(name, device="cpu").to(DEV)
+    out, err = run(pkg, w)
+    assert err == 0
+    assert_parity(out, oracle_of(w), what=name)
+
+
+CTX_POINTS = [1, 2, 3, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 300, 383,
+              384, 385, 447, 448, 449, 511, 512]
+
+
+@pytest.mark.parametrize("shape", ["d64", "d128", "d256"])
+def test_parity_context_sweep(pkg, shape):
+    """Contexts 1..512 on both sides of the 256-token split threshold, with
+    the threshold moved so each length also runs on the other path."""
+    base = workloads.make(f"ctx512_{shape}", device="cpu")
+    for L in CTX_POINTS:
+        w = workloads.Workload(**{**base.__dict__, "seq_lens": torch.tensor([L], dtype=torch.int32)})
+        ref = oracle_of(w)
+        wd = w.to(DEV)
+        for split_min in (0, 1, 1024):
+            out, err = run(pkg, wd, split_min=split_min)
+            assert err == 0
+            assert_parity(out, ref, what=(shape, L, split_min))
+
+
+def test_parity_batched(pkg):
+    w = workloads.make("batched", device=DEV)
+    out, err = run(pkg, w)
+    assert err == 0
+    assert_parity(out, oracle_of(w), what="batched")
+
+
+@pytest.mark.parametrize("name", ["long", "long_w4096"])
+def test_parity_long(pkg, name):
+    """Full size, launched as the benchmark launches it; for the full
+    context the oracle computes a sample of rows (every batch entry, heads
+    spread over all KV heads and group slots)."""
+    w = workloads.make(name, device=DEV)
+    out, err = run(pkg, w)
+    assert err == 0
+    if w.window:
+        assert_parity(out, oracle_of(w), what=name)
+    else:
+        Hq = w.num_q_heads
+        rows = np.array([b * Hq + hq for b in range(w.batch) for hq in (0, 9, 18, 27, 36, 45,
+                                                                          54, 63)])
+        assert_parity(out, oracle_of(w, rows=rows), rows=rows, what=name)
+
+
+# ------------------------------------------------------- bit-exact facts
+
+def small_pool(rng_seed, B, Hq, Hkv, D, PS, lens, decoys=4):
+    return workloads.make_custom("t", batch=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                                 page_size=PS, seq_lens=lens, seed=rng_seed, decoy_pages=decoys)
+
+
+@pytest.mark.parametrize("PS,D", [(16, 64), (64, 128), (8, 256), (128, 128)])
+def test_context_one_returns_v_row_bitwise(pkg, PS, D):
+    # window 1 attends the last position only: the weight is exactly 1
+    lens = [1, PS, PS + 1, 2 * PS - 1, 3 * PS + 5, 64, 65, 300]
+    w = small_pool(21, len(lens), 8, 2, D, PS, lens).to(DEV)
+    for split_min in (0, 1):
+        out, err = run(pkg, w, window=1, split_min=split_min)
+        assert err == 0
+        for b, L in enumerate(lens):
+            t = L - 1
+            phys = int(w.page_table[b, t // PS])
+            for hq in range(8):
+                v = w.v_pages[phys, t % PS, hq // 4]
+                assert torch.equal(out[b, hq], v), (PS, D, b, hq)
+
+
+def test_page_permutation_bitwise(pkg):
+    w = workloads.make("llama", device=DEV)
+    out1, _ = run(pkg, w)
+    P = w.k_pages.shape[0]
+    g = torch.Generator().manual_seed(7)
+    perm = torch.randperm(P, generator=g).to(DEV)
+    inv = torch.argsort(perm).to(torch.int32)
+    table2 = torch.where(w.page_table >= 0, inv[w.page_table.clamp(min=0).long()],
+                         w.page_table)
+    w2 = workloads.Workload(**{**w.__dict__, "k_pages": w.k_pages[perm].contiguous(),
+                               "v_pages": w.v_pages[perm].contiguous(),
+                               "page_table": table2.contiguous()})
+    out2, _ = run(pkg, w2)
+    assert torch.equal(out1, out2)
+
+
+@pytest.mark.parametrize("name", ["llama", "long_w4096"])
+def test_run_to_run_bitwise(pkg, name):
+    w = workloads.make(name, device=DEV)
+    first, _ = run(pkg, w)
+    for _ in range(10):
+        again, _ = run(pkg, w)
+        assert torch.equal(first, again)
+
+
+def test_batched_run_to_run_bitwise(pkg):
+    w = workloads.make("batched", device=DEV)
+    first, _ = run(pkg, w)
+    for _ in range(3):
+        again, _ = run(pkg, w)
+        assert torch.equal(first, again)
+
+
+def test_repeated_q_rows_give_identical_outputs(pkg):
+    w = workloads.make("llama", device=DEV)
+    q = w.q.clone()
+    q[:, 1] = q[:, 0]          # heads 0 and 1 share KV head 0
+    q[:, 13] = q[:, 12]        # heads 12 and 13 share KV head 3
+    w2 = workloads.Workload(**{**w.__dict__, "q": q})
+    out, _ = run(pkg, w2)
+    assert torch.equal(out[:, 0], out[:, 1]) and torch.equal(out[:, 12], out[:, 13])
+
+
+# ------------------------------------------------- paths and properties
+
+@pytest.mark.parametrize("chunk", [64, 128, 192, 1024, 3072])
+def test_forced_chunks_match_oracle(pkg, chunk):
+    w = workloads.make("sweep_d128", device="cpu")
+    ref = oracle_of(w)
+    out, err = run(pkg, w.to(DEV), force_chunk=chunk)
+    assert err == 0
+    assert_parity(out, ref, what=chunk)
+
+
+def test_window_equals_truncation(pkg):
+    W = 700
+    lens = [3060, 701, 700, 300, 1]
+    w = small_pool(22, len(lens), 32, 8, 128, 16, lens).to(DEV)
+    out, err = run(pkg, w, window=W)
+    assert err == 0
+    # the same positions copied into a fresh cache holding only the window
+    for b, L in enumerate(lens):
+        lo = max(0, L - W)
+        pos = torch.arange(lo, L, device=DEV)
+        phys = w.page_table[b, pos // 16].long()
+        krows = w.k_pages[phys, pos % 16]
+        vrows = w.v_pages[phys, pos % 16]
+        n = L - lo
+        npg = (n + 15) // 16
+        k2 = torch.zeros(npg * 16, 8, 128, dtype=torch.float16, device=DEV)
+        v2 = torch.zeros_like(k2)
+        k2[:n], v2[:n] = krows, vrows
+        t2 = torch.arange(npg, dtype=torch.int32, device=DEV)[None]
+        w2 = workloads.Workload(name="trunc", q=w.q[b:b + 1].contiguous(),
+                                k_pages=k2.view(npg, 16, 8, 128), v_pages=v2.view(npg, 16, 8, 128),
+                                page_table=t2, seq_lens=torch.tensor([n], dtype=torch.int32,
+                                                                      device=DEV),
+                                scale=w.scale)
+        trunc, _ = run(pkg, w2)
+        rel, mab, _ = compare(out[b:b + 1], trunc.float().cpu().numpy().astype(np.float64))
+        assert rel <= REL_L2 and mab <= MAX_ABS, (b, rel, mab)
+
+
+@pytest.mark.parametrize("PS", [8, 32, 128, 256])
+@pytest.mark.parametrize("D", [64, 128])
+def test_page_sizes(pkg, PS, D):
+    lens = [1000, 257, 3, 2048]
+    w = small_pool(23, len(lens), 16, 4, D, PS, lens)
+    out, err = run(pkg, w.to(DEV))
+    assert err == 0
+    assert_parity(out, oracle_of(w), what=(PS, D))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (12, 4), (20, 4), (32, 4), (7, 1)])
+def test_group_sizes(pkg, Hq, Hkv):
+    lens = [777, 100]
+    w = small_pool(24, len(lens), Hq, Hkv, 128, 16, lens)
+    out, err = run(pkg, w.to(DEV))
+    assert err == 0
+    assert_parity(out, oracle_of(w), what=(Hq, Hkv))
+
+
+def test_max_sequence_of_page_table(pkg):
+    # a sequence filling its whole page-table row, with the default grid bound
+    lens = [16 * 160, 5]
+    w = small_pool(25, len(lens), 8, 2, 128, 16, lens)
+    out, err = run(pkg, w.to(DEV), max_seq_len=None)
+    assert err == 0
+    assert_parity(out, oracle_of(w))
+
+
+# -------------------------------------------------------------- errors
+
+def test_device_errors_zero_only_bad_rows(pkg):
+    lens = [500, 0, 300, 400, 600]
+    w = small_pool(26, len(lens), 8, 2, 128, 16, lens).to(DEV)
+    cap = w.page_table.shape[1] * 16
+    table = w.page_table.clone()
+    table[2, 3] = w.k_pages.shape[0] + 5          # page id past the pool
+    table[3, 1] = -7                              # negative page id
+    seq = w.seq_lens.clone()
+    seq[4] = cap + 1                              # longer than the table
+    w2 = workloads.Workload(**{**w.__dict__, "page_table": table, "seq_lens": seq})
+    out, err = run(pkg, w2, max_seq_len=cap)
+    assert err & pkg.DEV_BAD_PAGE and err & pkg.DEV_BAD_LEN
+    assert torch.all(out[1:] == 0)
+    ref = oracle_of(w2, rows=np.arange(8))
+    assert_parity(out[0:1], ref)
+
+
+def test_length_above_hint_is_flagged(pkg):
+    lens = [2000, 100]
+    w = small_pool(27, len(lens), 8, 2, 128, 16, lens).to(DEV)
+    out, err = run(pkg, w, max_seq_len=1000)
+    assert err & pkg.DEV_OVER_HINT
+    assert torch.all(out[0] == 0)
+    assert_parity(out[1:], oracle_of(w, rows=np.arange(8, 16)))
+
+
+def test_empty_batch_entry(pkg):
+    lens = [0, 0]
+    w = small_pool(28, 2, 8, 2, 64, 16, [1, 1]).to(DEV)
+    w2 = workloads.Workload(**{**w.__dict__, "seq_lens": torch.zeros(2, dtype=torch.int32,
+                                                                      device=DEV)})
+    out, err = run(pkg, w2, max_seq_len=600)
+    assert err == 0 and torch.all(out == 0)
+    del lens
+
+
+# ---------------------------------------------------- ABI entry points
+
+def test_split_plus_combine_equals_decode_attn(pkg):
+    w = workloads.make("llama", device=DEV)
+    ref, _ = run(pkg, w)
+    out, ws = pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
+                                    w.scale, max_seq_len=w.max_seq_len())
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    pkg.decode_attn_combine(params, w.seq_lens, out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+def test_host_entry_point_equals_device_path(pkg):
+    w = workloads.make("sweep_d64", device="cpu")
+    ref, _ = run(pkg, w.to(DEV))
+    pin = lambda t: t.contiguous().pin_memory()
+    qh, kh, vh, th, lh = map(pin, (w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens))
+    out_h = torch.empty_like(qh).pin_memory()
+    d = [torch.empty_like(t, device=DEV) for t in (qh, kh, vh, th, lh, qh)]
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    ws = torch.empty(pkg.decode_attn_workspace_size(params, 0) + 256, dtype=torch.uint8,
+                     device=DEV)
+    pkg.decode_attn_host(params, qh, kh, vh, th, lh, out_h, *d, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref.cpu())
+
+
+def test_non_default_stream(pkg):
+    w = workloads.make("llama", device=DEV)
+    ref, _ = run(pkg, w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                              max_seq_len=w.max_seq_len())
+    s.synchronize()
+    assert torch.equal(out, ref)
