@@ -38,6 +38,7 @@ METRIC = "decode-attention effective KV-read TB/s (% of HBM peak); µs per decod
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD_DESC = {
     "long": "B=4, seq 131072 each, Hq=64, Hkv=8, D=128, page 64, full context",
+    "long_b1": "B=1, seq 131072, Hq=64, Hkv=8, D=128, page 64, full context",
     "long_w4096": "B=4, seq 131072 each, Hq=64, Hkv=8, D=128, page 64, window 4096",
     "batched": "B=64, Hq=32, Hkv=8, D=128, seq_lens U[1,8192], page 16",
     "llama": "B=1, Hq=32, Hkv=8, D=128, context 3060, page 16 (Llama-3.1-8B shape)",

@@ -87,7 +87,7 @@ def load_library():
                 f.restype = ctypes.c_int
             lib.decode_attn_combine.argtypes = [PP, P, P, P, sz, P, P]
             lib.decode_attn_combine.restype = ctypes.c_int
-            lib.decode_attn_host.argtypes = [PP] + [P] * 13 + [sz, P, sz, P, P]
+            lib.decode_attn_host.argtypes = [PP] + [P] * 12 + [sz, P, sz, P, P]
             lib.decode_attn_host.restype = ctypes.c_int
             lib.decode_attn_strerror.argtypes = [ctypes.c_int]
             lib.decode_attn_strerror.restype = ctypes.c_char_p

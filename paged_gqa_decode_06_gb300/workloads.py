@@ -142,6 +142,9 @@ CONFIGS = {
     # long context: 4 x 131072 tokens, 64/8 heads, PS 64 (1 GiB each for K and V)
     "long": dict(batch=4, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
                  seq_lens=[131072] * 4, seed=4),
+    # one sequence of the long-context case (512 MiB of K+V, still above L2)
+    "long_b1": dict(batch=1, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
+                    seq_lens=[131072], seed=4),
     "long_w4096": dict(batch=4, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
                        seq_lens=[131072] * 4, seed=4, window=4096),
 }

@@ -156,3 +156,24 @@ def test_plan_covers_every_length(pkg, max_len, units):
     assert plan.chunk_tokens * plan.max_shards >= max_len
     assert plan.chunk_tokens <= 1024 * min(PS, 64)   # page ids of one shard fit in smem
     assert plan.grid_x == plan.max_shards and plan.grid_y == Hkv and plan.grid_z == B
+
+
+def declared_arity():
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;",
+                             text, flags=re.M):
+            args = m.group(2).strip()
+            out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_header(pkg):
+    lib = pkg.load_library()
+    arity = declared_arity()
+    assert arity
+    for name, n in arity.items():
+        f = getattr(lib, name)
+        if f.argtypes is not None:
+            assert len(f.argtypes) == n, (name, len(f.argtypes), n)
