@@ -160,6 +160,33 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
 /* Static text for a return code. */
 const char* decode_attn_strerror(int status);
 
+/*
+ * ---- Variant that allocates nothing (the pages have no counterpart) ----
+ *
+ * decode_attn_static_scratch: the same step as decode_attn, for callers that
+ * cannot allocate device memory themselves (their device memory is held by
+ * another framework's allocator, they sit behind a plugin interface that
+ * passes only the call's tensors, or they must not pay cudaMalloc's implicit
+ * synchronisation).  The shard partials go to a fixed array of
+ * DECODE_ATTN_STATIC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  The caller still passes
+ * the inputs and the output (layouts, alignment and err_flag as for
+ * decode_attn).  The first call on a device looks up the array's device
+ * address on that device; make that first call before any stream capture.
+ * Plans whose partials need more than the array return
+ * DECODE_ATTN_ERR_SCRATCH_LIMIT without launching; decode_attn_workspace_size
+ * tells the need in advance.  All calls on a device share the array: calls
+ * whose GPU work can overlap (other streams, other host threads) race and
+ * must be serialised by the caller.  Nothing in the array needs clearing
+ * between calls.  Calls no cudaMalloc, cudaFree or allocating routine.
+ */
+#define DECODE_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
+#define DECODE_ATTN_ERR_SCRATCH_LIMIT (-11) /* partials above the static scratch size */
+int decode_attn_static_scratch(const decode_attn_params* p, const void* q, const void* k_pages,
+                               const void* v_pages, const int32_t* page_table,
+                               const int32_t* seq_lens, void* out, int32_t* err_flag,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ __all__ = [
     "decode_attn_host", "decode_attn_workspace_size", "decode_attn_make_plan",
     "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
+    "decode_attn_static_scratch",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
@@ -262,3 +263,41 @@ def decode_attn_host(params: DecodeAttnParams, q_host, k_host, v_host, table_hos
     if st:
         raise DecodeAttnError(st, "decode_attn_host")
     return out_host
+
+
+# ------------------------------------------- no-allocation variant
+
+def _static_scratch_fn():
+    f = load_library().decode_attn_static_scratch
+    if f.argtypes is None:
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.POINTER(DecodeAttnParams), P, P, P, P, P, P, P, P]
+        f.restype = ctypes.c_int
+    return f
+
+
+def decode_attn_static_scratch(q, k_pages, v_pages, page_table, seq_lens, scale: float,
+                               window: int = 0, out=None, max_seq_len: Optional[int] = None,
+                               err_flag=None, variant: int = VARIANT_AUTO, split_min: int = 0,
+                               force_chunk: int = 0, stream=None):
+    """decode_attn for callers that cannot allocate device memory: the shard
+    partials use the library's fixed 8 MiB device array instead of a
+    workspace (shared by all calls on a device; overlapping calls race).
+    Only ``out`` is created here when not given; pass it to allocate nothing."""
+    import torch
+    dev = q.device
+    for t, dt, n in ((q, torch.float16, "q"), (k_pages, torch.float16, "k_pages"),
+                     (v_pages, torch.float16, "v_pages"), (page_table, torch.int32, "page_table"),
+                     (seq_lens, torch.int32, "seq_lens")):
+        _check(t, dt, n, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, torch.float16, "out", dev)
+    p = make_params(q, k_pages, page_table, scale, window, max_seq_len, variant, split_min,
+                    force_chunk)
+    st = _static_scratch_fn()(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),
+                              _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(err_flag),
+                              _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_static_scratch")
+    return out

@@ -404,6 +404,9 @@ extern "C" const char* decode_attn_strerror(int status) {
     case DECODE_ATTN_ERR_CUDA: return "CUDA runtime error";
     case DECODE_ATTN_ERR_TENSOR_MAP: return "TMA descriptor for the K/V pool rejected";
     case DECODE_ATTN_ERR_VARIANT: return "kernel variant unavailable for this shape";
+    case DECODE_ATTN_ERR_SCRATCH_LIMIT:
+      return "partials exceed the library's static scratch (8 MiB); use decode_attn with a "
+             "workspace";
     default: return "unknown status";
   }
 }
