@@ -97,9 +97,17 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   const int G = p->num_q_heads / p->num_kv_heads;
   const int gp = next_pow2(G);
   int variant = p->variant;
-  if (variant == DECODE_ATTN_VARIANT_AUTO) variant = DECODE_ATTN_VARIANT_SIMT;
-  if (variant != DECODE_ATTN_VARIANT_SIMT) return DECODE_ATTN_ERR_VARIANT;
-  if (gp > 8) return DECODE_ATTN_ERR_VARIANT;
+  // the tensor-core variant measured faster on every shape (G = 4 and 8,
+  // D = 64..256); the CUDA-core variant stays selectable
+  if (variant == DECODE_ATTN_VARIANT_AUTO) variant = DECODE_ATTN_VARIANT_MMA;
+  int group_pad = gp;
+  if (variant == DECODE_ATTN_VARIANT_SIMT) {
+    if (gp > 8) return DECODE_ATTN_ERR_VARIANT;
+  } else if (variant == DECODE_ATTN_VARIANT_MMA) {
+    group_pad = gp <= 8 ? 8 : 16;  // one or two n8 tiles of heads
+  } else {
+    return DECODE_ATTN_ERR_VARIANT;
+  }
 
   const int64_t capacity = (int64_t)p->max_pages_per_seq * p->page_size;
   const int64_t max_len =
@@ -145,7 +153,7 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   if (max_shards > 65535) return DECODE_ATTN_ERR_SHAPE;
 
   plan->variant = variant;
-  plan->group_pad = gp;
+  plan->group_pad = group_pad;
   plan->tile_tokens = kTile;
   plan->chunk_tokens = (int32_t)chunk;
   plan->max_shards = (int32_t)max_shards;
@@ -194,6 +202,25 @@ int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params
   return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
 }
 
+// 4-D view (64 dims, D/64 chunks, kv head, P*PS token rows) with the 128-byte
+// swizzle: one box = box_t rows x 64 dims of one head, written to shared
+// memory as [box_t][64] with 16-byte chunk c of row t at chunk c ^ (t % 8).
+int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_attn_params* p,
+                             int box_t) {
+  auto fn = encode_fn();
+  if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
+  const int D = p->head_dim;
+  cuuint64_t dims[4] = {64, (cuuint64_t)D / 64, (cuuint64_t)p->num_kv_heads,
+                        (cuuint64_t)p->num_pages * p->page_size};
+  cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)p->num_kv_heads * D * 2};
+  cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_t};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
+}
+
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
 int plan_for_stream(const decode_attn_params* p, cudaStream_t stream, decode_attn_plan* plan) {
@@ -236,8 +263,10 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   if (p->batch == 0) return DECODE_ATTN_OK;
   SplitLaunch L;
   const int box_t = std::min(p->page_size, kTile);
-  int st = encode_pool_map(&L.tmap_k, k_pages, p, box_t);
-  if (!st) st = encode_pool_map(&L.tmap_v, v_pages, p, box_t);
+  auto encode = plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
+                                                         : encode_pool_map;
+  int st = encode(&L.tmap_k, k_pages, p, box_t);
+  if (!st) st = encode(&L.tmap_v, v_pages, p, box_t);
   if (st) return st;
   SplitArgs& a = L.args;
   a.q = static_cast<const __half*>(q);

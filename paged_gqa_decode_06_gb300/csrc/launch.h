@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "combine.cuh"
+#include "split_mma.cuh"
 #include "split_simt.cuh"
 
 namespace pgd {

@@ -1,0 +1,386 @@
+// Split decode-attention kernel, tensor-core variant.
+//
+// Same CTA shape, shard arithmetic, TMA producer and fixed-order epilogue as
+// the CUDA-core variant (split_simt.cuh); only the q.k and p.v products move
+// to mma.sync.m16n8k16 (fp16 x fp16 -> fp32), with tokens on the 16-row M
+// side and the G query heads of the group on the N side (N = 8 per tile, two
+// tiles for G up to 16):
+//   scores^T [16 tok x 8 heads] = K [16 tok x D] . Q^T [D x 8 heads]
+//   out^T    [D x 8 heads]     += V^T [D x 16 tok] . P^T [16 tok x 8 heads]
+// The score accumulator's fragment is transposed into the P^T operand with
+// movmatrix; P is split into an fp16 head and an fp16 remainder (two mma per
+// tile) so the weights keep about 22 bits, as the fp32 CUDA-core path does.
+//
+// Shared-memory tiles are [D/64][64 tokens][64 dims] with the 128-byte TMA
+// swizzle (16-byte chunk c of token row t lives at chunk c ^ (t % 8)), so
+// every ldmatrix of 8 token rows touches 8 distinct bank groups.
+#pragma once
+
+#include "split_simt.cuh"  // SplitArgs, zero_group_rows
+
+namespace pgd {
+
+template <int D>
+struct MmaCfg {
+  static constexpr int kWarps = 4;  // consumer warps, 16 tokens of each stage apiece
+  static constexpr int kThreads = (kWarps + 1) * 32;
+  static constexpr int kStages = (D == 64) ? 6 : 3;
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kRingBytes + 1024;
+  static constexpr int kChunkBytes = kTile * 128;  // one [64 tok][64 dims] sub-tile
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Byte offset of (token row t, dim d) inside a swizzled [D/64][64][64] tile.
+__device__ __forceinline__ uint32_t swz_offset(int t, int d) {
+  return (uint32_t)((d >> 6) * (kTile * 128) + t * 128 + ((((d >> 3) & 7) ^ (t & 7)) << 4));
+}
+
+template <int D, int NT8>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads)
+    split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+  using C = MmaCfg<D>;
+  constexpr int GP = 8 * NT8;  // padded heads of the group
+  constexpr int KS = D / 16;   // k-steps of q.k, m-tiles of p.v
+  constexpr int kWarps = C::kWarps;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ int32_t coord_s[kMaxPieces];
+  __shared__ float2 ml_s[kWarps][GP];
+  __shared__ int32_t bad_s;
+  __shared__ volatile int32_t abort_s;
+
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
+                               a.max_shards);
+  if (r.status != 0 || s >= r.nshards) {
+    if (s == 0) {
+      if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
+      if (!a.split) zero_group_rows<D, GP>(a, b, h);
+    }
+    return;
+  }
+
+  const int shard_lo = r.base + s * a.chunk;
+  const int lo = max(r.start, shard_lo);
+  const int hi = min(r.end, shard_lo + a.chunk);
+  const int n_tiles = (hi - shard_lo + kTile - 1) / kTile;
+  const int box_t = a.box_tokens;
+  const int pieces_per_tile = kTile / box_t;
+  const int n_pieces = n_tiles * pieces_per_tile;
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+
+  if (warp == kWarps) {
+    int bad = 0;
+    const int oob = a.num_pages * a.page_size;  // past the pool: TMA writes zeros
+    for (int i = lane; i < n_pieces; i += 32) {
+      const int ptok = shard_lo + i * box_t;
+      int coord = oob;
+      if (ptok < hi && ptok + box_t > lo) {
+        const int phys = a.page_table[(size_t)b * a.max_pages + (ptok >> a.page_shift)];
+        if (phys < 0 || phys >= a.num_pages) {
+          bad = 1;
+        } else {
+          coord = phys * a.page_size + (ptok & (a.page_size - 1));
+        }
+      }
+      coord_s[i] = coord;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      bad_s = bad;
+      abort_s = 0;
+      for (int st = 0; st < C::kStages; ++st) {
+        mbar_init(smem_u32(&full_bar[st]), 1);
+        mbar_init(smem_u32(&empty_bar[st]), kWarps);
+      }
+      fence_mbar_init();
+      if (bad) raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
+    }
+  }
+  __syncthreads();
+  const bool bad = bad_s != 0;
+
+  if (warp == kWarps) {
+    if (lane == 0 && !bad) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+      const uint32_t box_bytes = box_t * 128;  // one 64-dim slice of box_t rows
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % C::kStages;
+        if (i >= C::kStages &&
+            !mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) & 1) ^ 1)) {
+          abort_s = 1;
+          raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
+          break;
+        }
+        if (abort_s) break;
+        const uint32_t fb = smem_u32(&full_bar[st]);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
+        const uint32_t vdst = kdst + C::kTileBytes;
+        for (int pc = 0; pc < pieces_per_tile; ++pc) {
+          const int coord = coord_s[i * pieces_per_tile + pc];
+#pragma unroll
+          for (int dc = 0; dc < D / 64; ++dc) {
+            const uint32_t off = dc * C::kChunkBytes + pc * box_bytes;
+            tma_load_4d(kdst + off, &tmap_k, 0, dc, h, coord, fb);
+            tma_load_4d(vdst + off, &tmap_v, 0, dc, h, coord, fb);
+          }
+        }
+        issued = i + 1;
+      }
+      for (int i = max(0, issued - C::kStages); i < issued; ++i)
+        mbar_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int G = a.G;
+  const int gid = lane >> 2, tig = lane & 3;
+  // Q^T operand fragments, held for the whole shard
+  uint32_t qf[NT8][KS][2];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) {
+    const int head = 8 * j + gid;
+    const __half* qrow = a.q + ((size_t)b * a.Hq + h * G + head) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (head < G) {
+        qf[j][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
+        qf[j][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig);
+      } else {
+        qf[j][ks][0] = qf[j][ks][1] = 0u;
+      }
+    }
+  }
+  float acc[KS][NT8][4];
+#pragma unroll
+  for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
+  float m_run[NT8][2], l_part[NT8][2];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) {
+    m_run[j][0] = m_run[j][1] = -INFINITY;
+    l_part[j][0] = l_part[j][1] = 0.f;
+  }
+
+  // per-lane ldmatrix row offsets (the tile's token rows of this warp)
+  const int mat = lane >> 3, mrow = lane & 7;
+  const int k_tok = 16 * warp + mrow + ((mat & 1) ? 8 : 0);  // K: matrix bit 0 -> +8 tokens
+  const int k_dof = (mat & 2) ? 8 : 0;                       // K: matrix bit 1 -> +8 dims
+  const int v_tok = 16 * warp + mrow + ((mat & 2) ? 8 : 0);  // V: matrix bit 1 -> +8 tokens
+  const int v_dof = (mat & 1) ? 8 : 0;                       // V: matrix bit 0 -> +8 dims
+
+  for (int i = 0; i < n_tiles && !bad; ++i) {
+    const int st = i % C::kStages;
+    if (!mbar_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1)) {
+      abort_s = 1;
+      raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
+      break;
+    }
+    if (abort_s) break;
+    const int tok0 = shard_lo + i * kTile + 16 * warp;  // this warp's 16 positions
+    if (tok0 + 16 > lo && tok0 < hi) {
+      uint8_t* kt = ring + st * C::kStageBytes;
+      const uint32_t kbase = smem_u32(kt);
+      const uint32_t vbase = kbase + C::kTileBytes;
+      if (tok0 < lo || tok0 + 16 > hi) {
+        // rows of this block outside the range: clear their V rows so a
+        // zero weight never meets a non-finite cache value
+        uint8_t* vt = kt + C::kTileBytes;
+        for (int e = lane; e < 16 * (D / 8); e += 32) {
+          const int t = e / (D / 8), c = e % (D / 8);
+          const int tok = tok0 + t;
+          if (tok < lo || tok >= hi)
+            *reinterpret_cast<uint4*>(vt + swz_offset(16 * warp + t, c * 8)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      // scores^T = K . Q^T
+      float sc[NT8][4];
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t af[4];
+        ldmatrix_x4(af, kbase + swz_offset(k_tok, ks * 16 + k_dof));
+#pragma unroll
+        for (int j = 0; j < NT8; ++j) mma_f16_16816(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
+      }
+      // online softmax over this block's 16 positions
+      const bool ok_a = (tok0 + gid >= lo) && (tok0 + gid < hi);
+      const bool ok_b = (tok0 + gid + 8 >= lo) && (tok0 + gid + 8 < hi);
+      uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
+      bool rescale = false;
+      float alpha[NT8][2];
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) {
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool ok = (e < 2) ? ok_a : ok_b;
+          sc[j][e] = ok ? sc[j][e] * a.scale_log2 : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mx = fmaxf(sc[j][e], sc[j][e + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_new = fmaxf(m_run[j][e], mx);
+          alpha[j][e] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run[j][e] - m_new);
+          rescale |= alpha[j][e] != 1.f;
+          p[e] = (sc[j][e] == -INFINITY) ? 0.f : fast_exp2(sc[j][e] - m_new);
+          p[e + 2] = (sc[j][e + 2] == -INFINITY) ? 0.f : fast_exp2(sc[j][e + 2] - m_new);
+          l_part[j][e] = l_part[j][e] * alpha[j][e] + p[e] + p[e + 2];
+          m_run[j][e] = m_new;
+        }
+        // P^T operand: fp16 head and fp16 remainder, transposed by movmatrix
+        const uint32_t h0 = pack_f16x2(p[0], p[1]);
+        const uint32_t h1 = pack_f16x2(p[2], p[3]);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+        const uint32_t l0 = pack_f16x2(p[0] - f0.x, p[1] - f0.y);
+        const uint32_t l1 = pack_f16x2(p[2] - f1.x, p[3] - f1.y);
+        pb_hi[j][0] = movmatrix_trans(h0);
+        pb_hi[j][1] = movmatrix_trans(h1);
+        pb_lo[j][0] = movmatrix_trans(l0);
+        pb_lo[j][1] = movmatrix_trans(l1);
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+          for (int j = 0; j < NT8; ++j) {
+            acc[mi][j][0] *= alpha[j][0];
+            acc[mi][j][1] *= alpha[j][1];
+            acc[mi][j][2] *= alpha[j][0];
+            acc[mi][j][3] *= alpha[j][1];
+          }
+      }
+      // out^T += V^T . P^T
+#pragma unroll
+      for (int mi = 0; mi < KS; ++mi) {
+        uint32_t af[4];
+        ldmatrix_x4_trans(af, vbase + swz_offset(v_tok, mi * 16 + v_dof));
+#pragma unroll
+        for (int j = 0; j < NT8; ++j) {
+          mma_f16_16816(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
+          mma_f16_16816(acc[mi][j], af, pb_lo[j][0], pb_lo[j][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
+  }
+
+  // ---- merge the consumer warps in fixed order (deterministic) ----------
+#pragma unroll
+  for (int j = 0; j < NT8; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l = l_part[j][e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      l_part[j][e] = l;
+    }
+  named_barrier_sync(1, kWarps * 32);  // every consumer is done with the ring
+  float* acc_s = reinterpret_cast<float*>(ring);  // [kWarps][GP][D]
+  if (gid == 0) {
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        ml_s[warp][8 * j + 2 * tig + e] = make_float2(m_run[j][e], l_part[j][e]);
+  }
+#pragma unroll
+  for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      const int hd = 8 * j + 2 * tig, d = 16 * mi + gid;
+      float* base = acc_s + (warp * GP) * D;
+      base[hd * D + d] = acc[mi][j][0];
+      base[(hd + 1) * D + d] = acc[mi][j][1];
+      base[hd * D + d + 8] = acc[mi][j][2];
+      base[(hd + 1) * D + d + 8] = acc[mi][j][3];
+    }
+  named_barrier_sync(1, kWarps * 32);
+  const bool dead = bad || abort_s != 0;
+
+  for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
+    const int g = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml_s[w][g].x);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float2 ml = ml_s[w][g];
+      if (ml.y == 0.f) continue;
+      const float c = fast_exp2(ml.x - M);
+      L += c * ml.y;
+      O += c * acc_s[(w * GP + g) * D + d];
+    }
+    const size_t row = (size_t)b * a.Hq + h * G + g;
+    if (!a.split) {
+      a.out[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
+    } else {
+      const size_t slot = row * a.max_shards + s;
+      a.ws_acc[slot * D + d] = dead ? 0.f : O;
+      if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
+    }
+  }
+}
+
+}  // namespace pgd

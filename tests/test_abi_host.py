@@ -177,3 +177,22 @@ def test_binding_argtypes_match_header(pkg):
         f = getattr(lib, name)
         if f.argtypes is not None:
             assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+
+
+def test_variant_selection(pkg):
+    # explicit CUDA-core variant serves groups up to 8 heads
+    with pytest.raises(pkg.DecodeAttnError) as e:
+        pkg.decode_attn_make_plan(params(pkg, num_q_heads=64, num_kv_heads=4, variant=1), 152)
+    assert e.value.code == -10
+    # tensor-core variant: one n8 tile up to 8 heads, two up to 16
+    plan = pkg.decode_attn_make_plan(params(pkg, num_q_heads=64, num_kv_heads=4, variant=2), 152)
+    assert plan.variant == 2 and plan.group_pad == 16
+    plan = pkg.decode_attn_make_plan(params(pkg, num_q_heads=12, num_kv_heads=4, variant=2), 152)
+    assert plan.group_pad == 8
+    plan = pkg.decode_attn_make_plan(params(pkg, num_q_heads=12, num_kv_heads=4, variant=1), 152)
+    assert plan.variant == 1 and plan.group_pad == 4
+    with pytest.raises(pkg.DecodeAttnError):
+        pkg.decode_attn_make_plan(params(pkg, variant=7), 152)
+    # automatic choice is a pure function of the shape
+    a = pkg.decode_attn_make_plan(params(pkg), 152).variant
+    assert a in (1, 2) and a == pkg.decode_attn_make_plan(params(pkg), 152).variant

@@ -17,6 +17,8 @@ from paged_gqa_decode_06_gb300 import workloads
 pytestmark = pytest.mark.gpu
 
 REL_L2, MAX_ABS, ROW_REL = 5e-4, 2e-3, 1e-3
+SIMT, MMA = 1, 2
+VARIANTS = pytest.mark.parametrize("variant", [SIMT, MMA], ids=["simt", "mma"])
 
 
 @pytest.fixture(scope="module")
@@ -70,10 +72,11 @@ def oracle_of(w, rows=None, window=None):
 
 # ------------------------------------------------------------- configs
 
+@VARIANTS
 @pytest.mark.parametrize("name", ["tiny", "llama", "sweep_d64", "sweep_d128", "sweep_d256"])
-def test_parity_named(pkg, name):
+def test_parity_named(pkg, name, variant):
     w = workloads.make(name, device="cpu").to(DEV)
-    out, err = run(pkg, w)
+    out, err = run(pkg, w, variant=variant)
     assert err == 0
     assert_parity(out, oracle_of(w), what=name)
 
@@ -82,8 +85,9 @@ CTX_POINTS = [1, 2, 3, 15, 16, 17, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257
               384, 385, 447, 448, 449, 511, 512]
 
 
+@VARIANTS
 @pytest.mark.parametrize("shape", ["d64", "d128", "d256"])
-def test_parity_context_sweep(pkg, shape):
+def test_parity_context_sweep(pkg, shape, variant):
     """Contexts 1..512 on both sides of the 256-token split threshold, with
     the threshold moved so each length also runs on the other path."""
     base = workloads.make(f"ctx512_{shape}", device="cpu")
@@ -92,25 +96,27 @@ def test_parity_context_sweep(pkg, shape):
         ref = oracle_of(w)
         wd = w.to(DEV)
         for split_min in (0, 1, 1024):
-            out, err = run(pkg, wd, split_min=split_min)
+            out, err = run(pkg, wd, split_min=split_min, variant=variant)
             assert err == 0
             assert_parity(out, ref, what=(shape, L, split_min))
 
 
-def test_parity_batched(pkg):
+@VARIANTS
+def test_parity_batched(pkg, variant):
     w = workloads.make("batched", device=DEV)
-    out, err = run(pkg, w)
+    out, err = run(pkg, w, variant=variant)
     assert err == 0
     assert_parity(out, oracle_of(w), what="batched")
 
 
+@VARIANTS
 @pytest.mark.parametrize("name", ["long", "long_w4096"])
-def test_parity_long(pkg, name):
+def test_parity_long(pkg, name, variant):
     """Full size, launched as the benchmark launches it; for the full
     context the oracle computes a sample of rows (every batch entry, heads
     spread over all KV heads and group slots)."""
     w = workloads.make(name, device=DEV)
-    out, err = run(pkg, w)
+    out, err = run(pkg, w, variant=variant)
     assert err == 0
     if w.window:
         assert_parity(out, oracle_of(w), what=name)
@@ -128,13 +134,14 @@ def small_pool(rng_seed, B, Hq, Hkv, D, PS, lens, decoys=4):
                                  page_size=PS, seq_lens=lens, seed=rng_seed, decoy_pages=decoys)
 
 
+@VARIANTS
 @pytest.mark.parametrize("PS,D", [(16, 64), (64, 128), (8, 256), (128, 128)])
-def test_context_one_returns_v_row_bitwise(pkg, PS, D):
+def test_context_one_returns_v_row_bitwise(pkg, PS, D, variant):
     # window 1 attends the last position only: the weight is exactly 1
     lens = [1, PS, PS + 1, 2 * PS - 1, 3 * PS + 5, 64, 65, 300]
     w = small_pool(21, len(lens), 8, 2, D, PS, lens).to(DEV)
     for split_min in (0, 1):
-        out, err = run(pkg, w, window=1, split_min=split_min)
+        out, err = run(pkg, w, window=1, split_min=split_min, variant=variant)
         assert err == 0
         for b, L in enumerate(lens):
             t = L - 1
@@ -144,9 +151,10 @@ def test_context_one_returns_v_row_bitwise(pkg, PS, D):
                 assert torch.equal(out[b, hq], v), (PS, D, b, hq)
 
 
-def test_page_permutation_bitwise(pkg):
+@VARIANTS
+def test_page_permutation_bitwise(pkg, variant):
     w = workloads.make("llama", device=DEV)
-    out1, _ = run(pkg, w)
+    out1, _ = run(pkg, w, variant=variant)
     P = w.k_pages.shape[0]
     g = torch.Generator().manual_seed(7)
     perm = torch.randperm(P, generator=g).to(DEV)
@@ -156,53 +164,58 @@ def test_page_permutation_bitwise(pkg):
     w2 = workloads.Workload(**{**w.__dict__, "k_pages": w.k_pages[perm].contiguous(),
                                "v_pages": w.v_pages[perm].contiguous(),
                                "page_table": table2.contiguous()})
-    out2, _ = run(pkg, w2)
+    out2, _ = run(pkg, w2, variant=variant)
     assert torch.equal(out1, out2)
 
 
+@VARIANTS
 @pytest.mark.parametrize("name", ["llama", "long_w4096"])
-def test_run_to_run_bitwise(pkg, name):
+def test_run_to_run_bitwise(pkg, name, variant):
     w = workloads.make(name, device=DEV)
-    first, _ = run(pkg, w)
+    first, _ = run(pkg, w, variant=variant)
     for _ in range(10):
-        again, _ = run(pkg, w)
+        again, _ = run(pkg, w, variant=variant)
         assert torch.equal(first, again)
 
 
-def test_batched_run_to_run_bitwise(pkg):
+@VARIANTS
+def test_batched_run_to_run_bitwise(pkg, variant):
     w = workloads.make("batched", device=DEV)
-    first, _ = run(pkg, w)
+    first, _ = run(pkg, w, variant=variant)
     for _ in range(3):
-        again, _ = run(pkg, w)
+        again, _ = run(pkg, w, variant=variant)
         assert torch.equal(first, again)
 
 
-def test_repeated_q_rows_give_identical_outputs(pkg):
+@VARIANTS
+def test_repeated_q_rows_give_identical_outputs(pkg, variant):
     w = workloads.make("llama", device=DEV)
     q = w.q.clone()
     q[:, 1] = q[:, 0]          # heads 0 and 1 share KV head 0
     q[:, 13] = q[:, 12]        # heads 12 and 13 share KV head 3
     w2 = workloads.Workload(**{**w.__dict__, "q": q})
-    out, _ = run(pkg, w2)
+    out, _ = run(pkg, w2, variant=variant)
     assert torch.equal(out[:, 0], out[:, 1]) and torch.equal(out[:, 12], out[:, 13])
 
 
 # ------------------------------------------------- paths and properties
 
+@VARIANTS
 @pytest.mark.parametrize("chunk", [64, 128, 192, 1024, 3072])
-def test_forced_chunks_match_oracle(pkg, chunk):
+def test_forced_chunks_match_oracle(pkg, chunk, variant):
     w = workloads.make("sweep_d128", device="cpu")
     ref = oracle_of(w)
-    out, err = run(pkg, w.to(DEV), force_chunk=chunk)
+    out, err = run(pkg, w.to(DEV), force_chunk=chunk, variant=variant)
     assert err == 0
     assert_parity(out, ref, what=chunk)
 
 
-def test_window_equals_truncation(pkg):
+@VARIANTS
+def test_window_equals_truncation(pkg, variant):
     W = 700
     lens = [3060, 701, 700, 300, 1]
     w = small_pool(22, len(lens), 32, 8, 128, 16, lens).to(DEV)
-    out, err = run(pkg, w, window=W)
+    out, err = run(pkg, w, window=W, variant=variant)
     assert err == 0
     # the same positions copied into a fresh cache holding only the window
     for b, L in enumerate(lens):
@@ -222,26 +235,31 @@ def test_window_equals_truncation(pkg):
                                 page_table=t2, seq_lens=torch.tensor([n], dtype=torch.int32,
                                                                       device=DEV),
                                 scale=w.scale)
-        trunc, _ = run(pkg, w2)
+        trunc, _ = run(pkg, w2, variant=variant)
         rel, mab, _ = compare(out[b:b + 1], trunc.float().cpu().numpy().astype(np.float64))
         assert rel <= REL_L2 and mab <= MAX_ABS, (b, rel, mab)
 
 
+@VARIANTS
 @pytest.mark.parametrize("PS", [8, 32, 128, 256])
-@pytest.mark.parametrize("D", [64, 128])
-def test_page_sizes(pkg, PS, D):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_page_sizes(pkg, PS, D, variant):
     lens = [1000, 257, 3, 2048]
     w = small_pool(23, len(lens), 16, 4, D, PS, lens)
-    out, err = run(pkg, w.to(DEV))
+    out, err = run(pkg, w.to(DEV), variant=variant)
     assert err == 0
     assert_parity(out, oracle_of(w), what=(PS, D))
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (12, 4), (20, 4), (32, 4), (7, 1)])
-def test_group_sizes(pkg, Hq, Hkv):
+@VARIANTS
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (12, 4), (20, 4), (32, 4), (7, 1),
+                                    (48, 4), (64, 4), (13, 1)])
+def test_group_sizes(pkg, Hq, Hkv, variant):
+    if variant == SIMT and Hq // Hkv > 8:
+        pytest.skip("the CUDA-core variant serves groups of up to 8 heads")
     lens = [777, 100]
     w = small_pool(24, len(lens), Hq, Hkv, 128, 16, lens)
-    out, err = run(pkg, w.to(DEV))
+    out, err = run(pkg, w.to(DEV), variant=variant)
     assert err == 0
     assert_parity(out, oracle_of(w), what=(Hq, Hkv))
 
@@ -257,7 +275,8 @@ def test_max_sequence_of_page_table(pkg):
 
 # -------------------------------------------------------------- errors
 
-def test_device_errors_zero_only_bad_rows(pkg):
+@VARIANTS
+def test_device_errors_zero_only_bad_rows(pkg, variant):
     lens = [500, 0, 300, 400, 600]
     w = small_pool(26, len(lens), 8, 2, 128, 16, lens).to(DEV)
     cap = w.page_table.shape[1] * 16
@@ -267,17 +286,18 @@ def test_device_errors_zero_only_bad_rows(pkg):
     seq = w.seq_lens.clone()
     seq[4] = cap + 1                              # longer than the table
     w2 = workloads.Workload(**{**w.__dict__, "page_table": table, "seq_lens": seq})
-    out, err = run(pkg, w2, max_seq_len=cap)
+    out, err = run(pkg, w2, max_seq_len=cap, variant=variant)
     assert err & pkg.DEV_BAD_PAGE and err & pkg.DEV_BAD_LEN
     assert torch.all(out[1:] == 0)
     ref = oracle_of(w2, rows=np.arange(8))
     assert_parity(out[0:1], ref)
 
 
-def test_length_above_hint_is_flagged(pkg):
+@VARIANTS
+def test_length_above_hint_is_flagged(pkg, variant):
     lens = [2000, 100]
     w = small_pool(27, len(lens), 8, 2, 128, 16, lens).to(DEV)
-    out, err = run(pkg, w, max_seq_len=1000)
+    out, err = run(pkg, w, max_seq_len=1000, variant=variant)
     assert err & pkg.DEV_OVER_HINT
     assert torch.all(out[0] == 0)
     assert_parity(out[1:], oracle_of(w, rows=np.arange(8, 16)))
@@ -330,3 +350,14 @@ def test_non_default_stream(pkg):
                               max_seq_len=w.max_seq_len())
     s.synchronize()
     assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("name", ["llama", "long_w4096", "sweep_d256"])
+def test_variants_agree(pkg, name):
+    """Both variants compute the same real-valued result: their fp16 outputs
+    differ by at most one rounding of the output each."""
+    w = workloads.make(name, device=DEV)
+    a, _ = run(pkg, w, variant=SIMT)
+    b, _ = run(pkg, w, variant=MMA)
+    rel, mab, _ = compare(a, b.float().cpu().numpy().astype(np.float64))
+    assert rel <= REL_L2 and mab <= MAX_ABS
