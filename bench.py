@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--force-chunk", type=int, default=0)
+    ap.add_argument("--eager", action="store_true",
+                    help="launch each step from the host instead of replaying a CUDA graph")
     return ap.parse_args(argv)
 
 
@@ -295,7 +297,7 @@ def gpu_arm(args):
     props = torch.cuda.get_device_properties(dev)
     plan = pkg.decode_attn_make_plan(params, props.multi_processor_count)
     ws_bytes = pkg.decode_attn_workspace_size(params, local)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     out = torch.empty_like(w.q)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -303,50 +305,92 @@ def gpu_arm(args):
     resident = (w.k_pages.numel() + w.v_pages.numel()) * 2
     flush = kv_bytes < 2 * l2
     flush_buf = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev) if flush else None
+    flush_read = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev) if flush else None
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def flush_l2():
+        # write 4x L2 (evicts the step's data), then read another 4x L2 so the
+        # dirty lines are written back before the timed step, not during it
+        flush_buf.zero_()
+        flush_read.sum()
+
+    def split_call():
         pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
                               window=w.window, out=out, max_seq_len=max_len, workspace=ws,
                               err_flag=err, variant=args.variant, force_chunk=args.force_chunk)
-        if ev is not None:
-            ev[1].record(stream)
-        if plan.split:
-            pkg.decode_attn_combine(params, w.seq_lens, out, ws, err)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def step_call():
+        # one launch: the split kernel's last CTA per group merges the partials
+        split_call()
 
     for _ in range(args.warmup):
         if flush:
-            flush_buf.zero_()
-        step()
+            flush_l2()
+        step_call()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error bits {int(err.item())}")
 
+    # The step is captured once as a CUDA graph (the tickets' memset and the
+    # split kernel); replays carry no host launch work.  The roofline loop
+    # replays it again with events around every launch.
+    if args.eager:
+        run_step, run_split = step_call, split_call
+    else:
+        g_step, g_split = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            step_call()
+        with torch.cuda.graph(g_split):
+            split_call()
+        run_step, run_split = g_step.replay, g_split.replay
+        for _ in range(3):
+            run_step()
+            run_split()
+        torch.cuda.synchronize()
+
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def timed_loop(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        if flush:
+            for i in range(K):
+                flush_l2()  # between steps, outside the events
+                evs[i][0].record(stream)
+                fn()
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            per = [e0.elapsed_time(e1) for e0, e1 in evs]
+            return sum(per), per
+        e0, e1 = evs[0]
+        e0.record(stream)
+        for _ in range(K):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total = e0.elapsed_time(e1)
+        return total, None
+
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(K):
-        if flush:
-            flush_buf.zero_()  # outside the per-step events
-        step(evs[i])
-    torch.cuda.synchronize()
+    total_ms, _ = timed_loop(run_step)
     t_wall1 = time.time()
     barrier()
+    # split kernel alone, each launch bracketed by events on its stream
+    split_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(K)]
+    for i in range(K):
+        if flush:
+            flush_l2()
+        split_evs[i][0].record(stream)
+        run_split()
+        split_evs[i][1].record(stream)
+    torch.cuda.synchronize()
     sampler.stop()
-    if flush:
-        step_ms = [evs[i][0].elapsed_time(evs[i][2]) for i in range(K)]
-        total_ms = sum(step_ms)
-    else:
-        total_ms = evs[0][0].elapsed_time(evs[K - 1][2])
-    split_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    split_ms = [a.elapsed_time(b) for a, b in split_evs]
     split_avg_ms = statistics.mean(split_ms)
     ms_local = total_ms / K
     ms_max = max_over_ranks(ms_local, dev)
@@ -355,7 +399,6 @@ def gpu_arm(args):
     peak_gbs, peak_src = load_peak_hbm()
     split_achieved_gbs = kv_bytes / (split_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
-
     # ---- end to end from pinned host buffers through the C ABI
     e2e = None
     if args.e2e_steps > 0:
@@ -406,7 +449,7 @@ def gpu_arm(args):
             "dtype": "fp16 in / fp32 accumulate", "data": "synthetic (seeded N(0,1) fp16)",
             "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload],
                        "kv_bytes_per_step": kv_bytes, "resident_kv_bytes": resident,
-                       "l2": ("flushed between timed steps (write of 4x L2)" if flush else
+                       "l2": ("flushed between timed steps (write of 4x L2, then read of 4x L2)" if flush else
                               f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"),
                        "plan": plan.as_dict(), "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "split_simt_kernel" if plan.variant == 1
@@ -417,7 +460,8 @@ def gpu_arm(args):
                          "algorithmic_bytes_per_launch": kv_bytes,
                          "launch_us": split_avg_ms * 1e3},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": K * (2 if plan.split else 1),
+            "gpu_launches": K,
+            "launch_mode": "eager" if args.eager else "cuda graph replay",
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

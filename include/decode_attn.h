@@ -64,6 +64,8 @@ extern "C" {
 #define DECODE_ATTN_DEV_BAD_PAGE 2      /* page id outside [0, num_pages) in an attended range */
 #define DECODE_ATTN_DEV_OVER_HINT 4     /* seq_len beyond the max_seq_len the grid was planned for */
 #define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed */
+#define DECODE_ATTN_DEV_WORKSPACE 16    /* a group's shard ticket was not zero on entry:
+                                           the group's rows may be stale; clear and retry */
 
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
@@ -97,7 +99,8 @@ typedef struct decode_attn_plan {
   int32_t max_shards;        /* S_max: shards of the longest planned sequence */
   int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (shard, kv head, batch) */
   int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
-  size_t workspace_bytes;    /* partials: B*Hq*S_max*(D+2)*4 rounded; 0 if single pass */
+  size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
+                                each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;
 
 /*
@@ -113,10 +116,21 @@ int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sms, decode_a
 size_t decode_attn_workspace_size(const decode_attn_params* p, int device);
 
 /*
- * One decode step: plan, split kernel, and (when split) the ordered combine,
- * enqueued on `stream`.  workspace: device memory of at least
- * decode_attn_workspace_size() bytes, 256-byte aligned, owned by the caller;
- * its contents need no initialisation and are scratch after the call.
+ * One decode step: the host plan, then one split-kernel launch on `stream`.
+ * A split plan writes each shard's online-softmax partial to the workspace;
+ * the last CTA of each (sequence, KV head) group to finish (an atomic ticket,
+ * nothing waits) merges that group's partials in ascending shard order and
+ * writes out.  A single-pass plan writes out directly.
+ * workspace: device memory of at least decode_attn_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller.  Its first 64 KiB (more for plans
+ * with over 16384 (sequence, KV head) groups) hold one shard ticket per
+ * group, which must be zero when a split launch starts: zero the workspace
+ * when allocating it, or call decode_attn_workspace_clear().  Every
+ * completed call leaves the tickets zero again, and partials never use that
+ * region, so one zeroed buffer serves calls of any shape; after a call that
+ * reported DECODE_ATTN_DEV_TIMEOUT or DECODE_ATTN_DEV_WORKSPACE, clear it
+ * before reuse.  The rest of the workspace is scratch.  Calls sharing a
+ * workspace must not overlap on the GPU.
  * err_flag: nullable device int32, bits DECODE_ATTN_DEV_* are OR-ed in (the
  * caller clears it).  All tensor pointers must be 16-byte aligned.
  */
@@ -126,12 +140,15 @@ int decode_attn(const decode_attn_params* p, const void* q, const void* k_pages,
                 void* stream);
 
 /*
- * The two launches decode_attn makes, callable separately (e.g. to time the
- * split kernel alone).  decode_attn_split runs the shard kernel (and, for a
- * single-pass plan, writes out); decode_attn_combine merges the partials in
- * ascending shard order and is a no-op returning DECODE_ATTN_OK for a
- * single-pass plan.  Arguments as for decode_attn; the plan is recomputed
- * from *p and must be the same for both calls.
+ * decode_attn_split: the kernel launch decode_attn makes (same arguments,
+ * same result; kept as its own entry point so the split kernel can be timed
+ * or captured alone).  decode_attn_combine: re-merges the partials that the
+ * last split launch with this workspace left behind into out, in ascending
+ * shard order, as a separate kernel launched as a programmatic dependent of
+ * the preceding kernel on the stream; it runs the same merge code as the
+ * split kernel's last CTAs and gives the same bits.  A no-op returning
+ * DECODE_ATTN_OK for a single-pass plan.  The plan is recomputed from *p and
+ * must match the split call's.
  */
 int decode_attn_split(const decode_attn_params* p, const void* q, const void* k_pages,
                       const void* v_pages, const int32_t* page_table, const int32_t* seq_lens,
@@ -157,6 +174,11 @@ int decode_attn_host(const decode_attn_params* p, const void* q_host, const void
                      size_t kv_bytes_to_copy, void* workspace, size_t workspace_bytes,
                      int32_t* err_flag, void* stream);
 
+/* Zeroes the shard tickets of a workspace sized for *p (an async memset on
+ * `stream`); DECODE_ATTN_OK without work for a single-pass plan. */
+int decode_attn_workspace_clear(const decode_attn_params* p, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Static text for a return code. */
 const char* decode_attn_strerror(int status);
 
@@ -177,8 +199,9 @@ const char* decode_attn_strerror(int status);
  * DECODE_ATTN_ERR_SCRATCH_LIMIT without launching; decode_attn_workspace_size
  * tells the need in advance.  All calls on a device share the array: calls
  * whose GPU work can overlap (other streams, other host threads) race and
- * must be serialised by the caller.  Nothing in the array needs clearing
- * between calls.  Calls no cudaMalloc, cudaFree or allocating routine.
+ * must be serialised by the caller.  The array starts zeroed, and every
+ * completed call leaves the shard tickets it keeps there at zero; nothing
+ * needs clearing by the caller.  Calls no cudaMalloc, cudaFree or allocating routine.
  */
 #define DECODE_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
 #define DECODE_ATTN_ERR_SCRATCH_LIMIT (-11) /* partials above the static scratch size */

@@ -25,11 +25,11 @@ __all__ = [
     "decode_attn_host", "decode_attn_workspace_size", "decode_attn_make_plan",
     "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
-    "decode_attn_static_scratch",
+    "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
-DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -90,6 +90,8 @@ def load_library():
             lib.decode_attn_combine.restype = ctypes.c_int
             lib.decode_attn_host.argtypes = [PP] + [P] * 12 + [sz, P, sz, P, P]
             lib.decode_attn_host.restype = ctypes.c_int
+            lib.decode_attn_workspace_clear.argtypes = [PP, P, sz, P]
+            lib.decode_attn_workspace_clear.restype = ctypes.c_int
             lib.decode_attn_strerror.argtypes = [ctypes.c_int]
             lib.decode_attn_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -131,6 +133,16 @@ def decode_attn_workspace_size(params: DecodeAttnParams, device: int) -> int:
     return int(load_library().decode_attn_workspace_size(ctypes.byref(params), int(device)))
 
 
+def decode_attn_workspace_clear(params: DecodeAttnParams, workspace, stream=None) -> None:
+    """Zeroes the workspace's shard tickets (needed once for a workspace that
+    was not allocated zero-filled, or after a DEV_TIMEOUT / DEV_WORKSPACE)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load_library().decode_attn_workspace_clear(ctypes.byref(params), _ptr(workspace),
+                                                    nbytes, _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_workspace_clear")
+
+
 # ------------------------------------------------------------ torch glue
 
 _ws_cache: dict = {}
@@ -143,7 +155,9 @@ def _workspace(device, nbytes: int):
     key = (device.index if device.index is not None else torch.cuda.current_device())
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        # zero-filled: its shard tickets must start at zero (the kernels leave
+        # them zero after every completed call)
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
 

@@ -17,9 +17,8 @@ namespace {
 
 constexpr int kDefaultSplitMin = 256;
 constexpr int kMaxDevices = 64;
-// Planner cost of one CTA beyond its tokens (launch, page ids, first TMA
-// round trip, partial write), in tokens of streaming.
-constexpr int kCtaOverheadTokens = 64;
+constexpr int kMinChunk = 128;        // shortest shard the planner picks, tokens
+constexpr int kLargeChunkCap = 2048;  // longest shard for large work, unless span / 16
 constexpr int kSmemPerSm = 228 * 1024;
 
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -62,6 +61,16 @@ int check_params(const decode_attn_params* p) {
   if (p->num_q_heads / p->num_kv_heads > 16) return DECODE_ATTN_ERR_GROUP;
   if (!std::isfinite(p->scale)) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
+}
+
+// The shard tickets (one int32 per (sequence, KV head)) sit in a region at
+// the start of every workspace that partials never use, 64 KiB unless a plan
+// has more groups: a zero-filled workspace therefore stays valid across calls
+// with different shapes, since every completed call leaves its tickets zero.
+constexpr size_t kTicketRegion = 64 * 1024;
+size_t ticket_region_bytes(const decode_attn_params* p) {
+  const size_t need = ((size_t)p->batch * p->num_kv_heads * 4 + 255) / 256 * 256;
+  return need > kTicketRegion ? need : kTicketRegion;
 }
 
 int next_pow2(int x) {
@@ -127,26 +136,27 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   } else if (attended <= split_min) {
     chunk = round_up(span, kTile);  // one shard covers the whole range
   } else {
-    // choose the shard count minimising (waves of CTAs) x (tokens per CTA +
-    // fixed cost): CTAs = units * S, all of equal length for the longest
-    // sequence; ties go to fewer shards (fewer partials to merge)
+    // Shard count from the work bound (every (sequence, KV head) unit at the
+    // longest length) and the CTA slots (SMs x resident CTAs), calibrated on
+    // GB300 sweeps of the chunk size:
+    //  * small work (up to 1 MiB per slot): one wave, as many shards as fit,
+    //    chunks of at least 128 tokens -- a second wave costs a second
+    //    prologue (length, page ids, first TMA round trip) on a short step;
+    //  * large work: about 1.7 waves of CTAs, fewer prologues while DRAM stays
+    //    saturated to the end; chunks capped at max(2048, span / 16) tokens
+    //    so that batches of mixed lengths still cut into balanced pieces.
     const int64_t units = std::max<int64_t>(1, (int64_t)p->batch * p->num_kv_heads);
     const int64_t slots = (int64_t)num_sms * ctas_per_sm;
-    const int64_t s_hi = std::max<int64_t>(1, ceil_div(span, kTile));
-    int64_t best_cost = INT64_MAX;
-    chunk = round_up(span, kTile);
-    for (int64_t S = 1; S <= s_hi; ++S) {
-      const int64_t c = round_up(ceil_div(span, S), kTile);
-      if (c > max_chunk) continue;
-      const int64_t s_eff = ceil_div(span, c);
-      if (s_eff != S) continue;  // same chunk as a smaller S
-      const int64_t waves = ceil_div(units * s_eff, slots);
-      const int64_t cost = waves * (c + kCtaOverheadTokens);
-      if (cost < best_cost) {
-        best_cost = cost;
-        chunk = c;
-      }
+    const int64_t work_bytes = units * span * 4 * p->head_dim;
+    int64_t S;
+    if (work_bytes <= slots * (int64_t(1) << 20)) {
+      S = std::max<int64_t>(1, std::min(slots / units, ceil_div(span, kMinChunk)));
+    } else {
+      const int64_t target = std::max<int64_t>(1, (17 * slots + 5 * units) / (10 * units));
+      const int64_t cap = std::max<int64_t>(kLargeChunkCap, round_up(ceil_div(span, 16), kTile));
+      S = std::max(target, ceil_div(span, cap));
     }
+    chunk = std::min(round_up(ceil_div(span, S), kTile), max_chunk);
   }
   if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
   const int64_t max_shards = ceil_div(span, chunk);
@@ -163,8 +173,10 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->grid_z = p->batch;
   plan->ctas_per_sm = ctas_per_sm;
   if (plan->split) {
+    // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
     const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)max_shards;
-    plan->workspace_bytes = round_up(rows * sizeof(float2), 256) + rows * p->head_dim * 4;
+    plan->workspace_bytes = ticket_region_bytes(p) + round_up(rows * sizeof(float2), 256) +
+                            round_up(rows * p->head_dim * 4, 256);
   }
   return DECODE_ATTN_OK;
 }
@@ -238,19 +250,27 @@ int plan_for_stream(const decode_attn_params* p, cudaStream_t stream, decode_att
 struct Workspace {
   float2* ml;
   float* acc;
+  int32_t* counters;
+  size_t counter_bytes;
 };
 
 int workspace_views(const decode_attn_params* p, const decode_attn_plan& plan, void* ws,
                     size_t ws_bytes, Workspace* out) {
   out->ml = nullptr;
   out->acc = nullptr;
+  out->counters = nullptr;
+  out->counter_bytes = 0;
   if (!plan.split) return DECODE_ATTN_OK;
   if (!ws || ws_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
     return DECODE_ATTN_ERR_WORKSPACE;
   const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)plan.max_shards;
-  out->ml = reinterpret_cast<float2*>(ws);
-  out->acc = reinterpret_cast<float*>(static_cast<char*>(ws) +
-                                      round_up(rows * sizeof(float2), 256));
+  char* base = static_cast<char*>(ws);
+  const size_t tickets = ticket_region_bytes(p);
+  const size_t ml_bytes = round_up(rows * sizeof(float2), 256);
+  out->counters = reinterpret_cast<int32_t*>(base);
+  out->counter_bytes = tickets;
+  out->ml = reinterpret_cast<float2*>(base + tickets);
+  out->acc = reinterpret_cast<float*>(base + tickets + ml_bytes);
   return DECODE_ATTN_OK;
 }
 
@@ -275,6 +295,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.out = static_cast<__half*>(out);
   a.ws_acc = ws.acc;
   a.ws_ml = ws.ml;
+  a.counters = ws.counters;
   a.err = err_flag;
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
@@ -293,6 +314,8 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.group_pad = plan.group_pad;
   L.variant = plan.variant;
   L.stream = stream;
+  // the shard tickets are zero on entry: the last CTA of each group clears
+  // its own, so a workspace cleared once stays clear across calls
   switch (p->head_dim) {
     case 64: return cuda_status(launch_split_d64(L));
     case 128: return cuda_status(launch_split_d128(L));
@@ -310,6 +333,7 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
   a.out = static_cast<__half*>(out);
   a.B = p->batch;
   a.Hq = p->num_q_heads;
+  a.G = p->num_q_heads / p->num_kv_heads;
   a.capacity = p->max_pages_per_seq * p->page_size;
   a.window = p->window > 0 ? p->window : 0;
   a.chunk = plan.chunk_tokens;
@@ -379,9 +403,8 @@ extern "C" int decode_attn(const decode_attn_params* p, const void* q, const voi
   if ((st = check_tensors(q, k_pages, v_pages, page_table, seq_lens, out))) return st;
   Workspace ws;
   if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
-  st = run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s);
-  if (st) return st;
-  return run_combine(p, plan, seq_lens, out, ws, s);
+  // the split kernel's last CTA per group merges the partials (no second launch)
+  return run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s);
 }
 
 extern "C" int decode_attn_host(const decode_attn_params* p, const void* q_host,
@@ -418,6 +441,18 @@ extern "C" int decode_attn_host(const decode_attn_params* p, const void* q_host,
   if (st) return st;
   e = cudaMemcpyAsync(out_host, d_out, q_bytes, cudaMemcpyDeviceToHost, s);
   return cuda_status(e);
+}
+
+extern "C" int decode_attn_workspace_clear(const decode_attn_params* p, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  decode_attn_plan plan;
+  int st = plan_for_stream(p, s, &plan);
+  if (st) return st;
+  if (!plan.split) return DECODE_ATTN_OK;
+  Workspace ws;
+  if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
+  return cuda_status(cudaMemsetAsync(ws.counters, 0, ws.counter_bytes, s));
 }
 
 extern "C" const char* decode_attn_strerror(int status) {

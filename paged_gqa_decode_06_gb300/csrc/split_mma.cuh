@@ -90,6 +90,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   __shared__ int32_t bad_s;
   __shared__ volatile int32_t abort_s;
 
+  // the combine launched after this grid may be scheduled now; it waits for
+  // this grid's partials with griddepcontrol.wait before reading them
+  grid_launch_dependents();
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
@@ -97,7 +100,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   if (r.status != 0 || s >= r.nshards) {
     if (s == 0) {
       if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
-      if (!a.split) zero_group_rows<D, GP>(a, b, h);
+      zero_group_rows<D, GP>(a, b, h);
     }
     return;
   }
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
     }
   }
+  if (a.split) merge_if_last<D>(a, r, b, h, ring, kWarps * 32);
 }
 
 }  // namespace pgd

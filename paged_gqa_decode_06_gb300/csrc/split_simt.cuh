@@ -24,6 +24,7 @@
 // and exponentiated with ex2.
 #pragma once
 
+#include "combine.cuh"  // CombineArgs, grid_launch_dependents
 #include "device_common.cuh"
 
 namespace pgd {
@@ -35,6 +36,7 @@ struct SplitArgs {
   __half* out;                // [B][Hq][D]          (single pass)
   float* ws_acc;              // [B*Hq*S_max][D]     (split)
   float2* ws_ml;              // [B*Hq*S_max] (m, l) (split; l = -1 marks a bad row)
+  int32_t* counters;          // [B*Hkv] shards finished per group (split; zero on entry)
   int32_t* err;               // nullable
   int32_t Hq, Hkv, G;
   int32_t max_pages, num_pages, page_size, page_shift, box_tokens;
@@ -101,6 +103,42 @@ __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h
   }
 }
 
+// Split path epilogue, run by the consumer threads [0, nthreads) after this
+// CTA's partial is written: the last CTA of the group to finish (an atomic
+// ticket; no CTA ever waits on another) merges the group's partials into the
+// output in ascending shard order and clears the ticket for the next call.
+template <int D>
+__device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange& r, int b, int h,
+                                              uint8_t* smem, int nthreads) {
+  __shared__ int is_last_s;
+  __threadfence();  // this thread's partial writes, visible GPU-wide
+  named_barrier_sync(1, nthreads);
+  int32_t* ticket = a.counters + (size_t)b * a.Hkv + h;
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(ticket, 1);
+    if (old < 0 || old >= r.nshards) raise_error(a.err, DECODE_ATTN_DEV_WORKSPACE);
+    is_last_s = old == r.nshards - 1;
+  }
+  named_barrier_sync(1, nthreads);
+  if (!is_last_s) return;
+  __threadfence();
+  CombineArgs c;
+  c.seq_lens = a.seq_lens;
+  c.ws_acc = a.ws_acc;
+  c.ws_ml = a.ws_ml;
+  c.out = a.out;
+  c.B = 0;
+  c.Hq = a.Hq;
+  c.G = a.G;
+  c.capacity = a.max_pages * a.page_size;
+  c.window = a.window;
+  c.chunk = a.chunk;
+  c.max_shards = a.max_shards;
+  merge_group<D>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem,
+                 [nthreads] { named_barrier_sync(1, nthreads); });
+  if (threadIdx.x == 0) *ticket = 0;
+}
+
 template <int D, int GP>
 __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
     split_simt_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -121,16 +159,19 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   __shared__ int32_t bad_s;
   __shared__ volatile int32_t abort_s;
 
+  // the combine launched after this grid may be scheduled now; it waits for
+  // this grid's partials with griddepcontrol.wait before reading them
+  grid_launch_dependents();
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
                                a.max_shards);
   if (r.status != 0 || s >= r.nshards) {
-    // nothing to stream: report a bad length once; a single pass still owns
-    // its output rows (zero for an empty or invalid range)
+    // nothing to stream: report a bad length once; shard 0 owns the group's
+    // output rows (zero for an empty or invalid range)
     if (s == 0) {
       if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
-      if (!a.split) zero_group_rows<D, GP>(a, b, h);
+      zero_group_rows<D, GP>(a, b, h);
     }
     return;
   }
@@ -335,6 +376,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
       if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
     }
   }
+  if (a.split) merge_if_last<D>(a, r, b, h, ring, kWarps * 32);
 }
 
 }  // namespace pgd

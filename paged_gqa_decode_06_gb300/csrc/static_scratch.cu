@@ -18,10 +18,12 @@
 // routine is used here.
 //
 // Every call on a device shares the one array and leaves its contents behind.
-// Nothing in it needs to start at zero: the split kernel writes every partial
-// the combine reads within the same call.  Calls whose work overlaps on the
-// GPU (different streams, or different host threads) race on the array and
-// must be serialised by the caller.
+// The only part that must start at zero, the per-group shard tickets, starts
+// zeroed (a __device__ array is zero-initialised at module load) and every
+// completed call leaves it zero again; every partial the merge reads is
+// written earlier in the same call.  Calls
+// whose work overlaps on the GPU (different streams, or different host
+// threads) race on the array and must be serialised by the caller.
 #include <cuda_runtime.h>
 
 #include <mutex>

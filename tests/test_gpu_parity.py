@@ -334,7 +334,7 @@ def test_host_entry_point_equals_device_path(pkg):
     out_h = torch.empty_like(qh).pin_memory()
     d = [torch.empty_like(t, device=DEV) for t in (qh, kh, vh, th, lh, qh)]
     params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
-    ws = torch.empty(pkg.decode_attn_workspace_size(params, 0) + 256, dtype=torch.uint8,
+    ws = torch.zeros(pkg.decode_attn_workspace_size(params, 0) + 256, dtype=torch.uint8,
                      device=DEV)
     pkg.decode_attn_host(params, qh, kh, vh, th, lh, out_h, *d, ws)
     torch.cuda.synchronize()
@@ -361,3 +361,62 @@ def test_variants_agree(pkg, name):
     b, _ = run(pkg, w, variant=MMA)
     rel, mab, _ = compare(a, b.float().cpu().numpy().astype(np.float64))
     assert rel <= REL_L2 and mab <= MAX_ABS
+
+
+@pytest.mark.parametrize("name", ["llama", "long_w4096", "tiny"])
+def test_cuda_graph_capture_of_a_step(pkg, name):
+    """A decode step captured once as a CUDA graph (split kernel, then the
+    combine as a programmatic dependent launch) replays to the same bits as
+    the eager call, also after the inputs change in place."""
+    w = workloads.make(name, device=DEV)
+    ref, _ = run(pkg, w)
+    out = torch.empty_like(w.q)
+    kw = dict(window=w.window, out=out, max_seq_len=w.max_seq_len())
+    pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale, **kw)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale, **kw)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    # new query values in the same buffer: the replay reads them
+    w.q.copy_(torch.flip(w.q, dims=[1]))
+    ref2, _ = run(pkg, w)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2)
+
+
+@VARIANTS
+def test_more_shards_than_one_staged_block(pkg, variant):
+    """64-token shards over 20000 positions: 313 shards per row, more than the
+    combine stages in shared memory at once."""
+    lens = [20000, 700]
+    w = small_pool(29, len(lens), 16, 2, 64, 32, lens)
+    out, err = run(pkg, w.to(DEV), force_chunk=64, variant=variant)
+    assert err == 0
+    assert_parity(out, oracle_of(w))
+
+
+def test_dirty_workspace_is_detected_and_clearable(pkg):
+    """Shard tickets that are not zero on entry raise DEV_WORKSPACE (the
+    group's rows may then be stale); decode_attn_workspace_clear fixes it."""
+    w = workloads.make("llama", device=DEV)
+    ref, _ = run(pkg, w)
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    ws = torch.full((pkg.decode_attn_workspace_size(params, 0),), 0x7F, dtype=torch.uint8,
+                    device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                    max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkg.DEV_WORKSPACE
+    pkg.decode_attn_workspace_clear(params, ws)
+    err.zero_()
+    for _ in range(2):  # a completed call leaves the tickets clear
+        out = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                              max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0 and torch.equal(out, ref)
