@@ -65,6 +65,8 @@ def _bind(lib):
     lib.oracle_partial_f64.restype = ctypes.c_int
     lib.oracle_merge_f64.argtypes = [i32, i32, P, P, P, P]
     lib.oracle_merge_f64.restype = None
+    lib.oracle_kv_append_u16.argtypes = [ctypes.POINTER(OracleShape), P, P, P, P, P, P, P]
+    lib.oracle_kv_append_u16.restype = ctypes.c_int
     return lib
 
 
@@ -187,6 +189,26 @@ def _merge(lib, ms, ls, accs):
     return out
 
 
+def _kv_append(lib, k_new, v_new, positions, page_table, k_pages, v_pages):
+    """Returns new (k_pages, v_pages) uint16 arrays with the step's rows
+    k_new/v_new [B,Hkv,D] written at positions[b] (inputs untouched), and the
+    per-sequence error flags."""
+    ka = _as_u16(k_pages).copy()
+    va = _as_u16(v_pages).copy()
+    kn, vn = _as_u16(k_new), _as_u16(v_new)
+    pos, pt = _as_i32(positions), _as_i32(page_table)
+    P_, PS, Hkv, D = ka.shape
+    B = pt.shape[0]
+    assert kn.shape == (B, Hkv, D) and vn.shape == (B, Hkv, D)
+    sh = OracleShape(B, Hkv, Hkv, D, PS, pt.shape[1], P_)
+    err = np.zeros(max(B, 1), dtype=np.int32)
+    st = lib.oracle_kv_append_u16(ctypes.byref(sh), _ptr(kn), _ptr(vn), _ptr(pos), _ptr(pt),
+                                  _ptr(ka), _ptr(va), _ptr(err))
+    if st < 0:
+        raise ValueError("oracle: bad shape")
+    return ka, va, err[:B]
+
+
 class Oracle:
     """The oracle's entry points bound to one compiled library."""
 
@@ -204,6 +226,9 @@ class Oracle:
 
     def merge(self, *a, **k):
         return _merge(self.lib, *a, **k)
+
+    def kv_append(self, *a, **k):
+        return _kv_append(self.lib, *a, **k)
 
 
 def default() -> Oracle:
@@ -225,3 +250,8 @@ def partial(*a, **k):
 
 def merge(*a, **k):
     return _merge(_load(), *a, **k)
+
+
+def kv_append(*a, **k):
+    """See ``_kv_append``."""
+    return _kv_append(_load(), *a, **k)

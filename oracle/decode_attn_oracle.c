@@ -294,3 +294,55 @@ void oracle_merge_f64(int32_t n, int32_t D, const double* m, const double* l, co
   }
   for (int d = 0; d < D; ++d) out[d] /= L;
 }
+
+/* ---- paged K/V append ---------------------------------------------------- */
+
+/*
+ * idle-intelligence/llm-web pull request 8, suffix-prefill commit: new K/V
+ * rows are scattered into the cache at their positions after the resident
+ * prefix (the step before attention reads them).  For every b with
+ * positions[b] >= 0 and every KV head h:
+ *   k_pages[page_table[b][t / PS]][t % PS][h][:] = k_new[b][h][:],  t = positions[b]
+ * (likewise v).  A position < 0 means no new row for that sequence.  A
+ * position >= max_pages * PS or a page id outside [0, P) is invalid: nothing
+ * is written for that sequence and row_err[b] (nullable) is set.  Plain
+ * element copies of the fp16 bit patterns.  Returns the number of invalid
+ * sequences, -1 for a bad shape.
+ */
+int oracle_kv_append_u16(const oracle_shape* sh, const uint16_t* k_new, const uint16_t* v_new,
+                         const int32_t* positions, const int32_t* page_table, uint16_t* k_pages,
+                         uint16_t* v_pages, int32_t* row_err) {
+  if (!shape_ok(sh)) return -1;
+  int bad = 0;
+  for (int b = 0; b < sh->batch; ++b) {
+    int64_t t = positions[b];
+    int err = 0;
+    if (t >= 0) {
+      int64_t cap = (int64_t)sh->max_pages * sh->page_size;
+      if (t >= cap) {
+        err = 1;
+      } else {
+        int32_t phys = page_table[(int64_t)b * sh->max_pages + t / sh->page_size];
+        if (phys < 0 || phys >= sh->num_pages) err = 1;
+      }
+      if (!err) {
+        for (int h = 0; h < sh->num_kv_heads; ++h) {
+          /* kv_row is const; the same offset arithmetic written out here */
+          int32_t phys = page_table[(int64_t)b * sh->max_pages + t / sh->page_size];
+          int64_t off =
+              (((int64_t)phys * sh->page_size + t % sh->page_size) * sh->num_kv_heads + h) *
+              sh->head_dim;
+          const uint16_t* kn = k_new + ((int64_t)b * sh->num_kv_heads + h) * sh->head_dim;
+          const uint16_t* vn = v_new + ((int64_t)b * sh->num_kv_heads + h) * sh->head_dim;
+          for (int d = 0; d < sh->head_dim; ++d) {
+            k_pages[off + d] = kn[d];
+            v_pages[off + d] = vn[d];
+          }
+        }
+      }
+    }
+    if (row_err) row_err[b] = err;
+    bad += err;
+  }
+  return bad;
+}

@@ -268,9 +268,46 @@ def check_invalid_rows(o):
     assert np.any(out[0] != 0)
 
 
+def check_kv_append(o):
+    """Scatter of the step's rows: equals numpy fancy-index assignment; the
+    rows read back through the table are the new rows bit for bit; every
+    other slot is untouched; invalid positions write nothing and are flagged."""
+    rng = np.random.default_rng(20)
+    lens = [13, 5, 16, 1]
+    PS, Hkv, D = 4, 3, 8
+    q, k, v, t, L = rand_case(rng, 4, 6, Hkv, D, PS, lens, max_pages=5)
+    kn = rng.standard_normal((4, Hkv, D)).astype(np.float16)
+    vn = rng.standard_normal((4, Hkv, D)).astype(np.float16)
+    pos = np.array([13, -1, 15, 0], dtype=np.int32)   # b=2 overwrites its last slot
+    k2, v2, err = o.kv_append(kn, vn, pos, t, k, v)
+    ref_k, ref_v = k.copy(), v.copy()
+    for b in range(4):
+        if pos[b] < 0:
+            continue
+        ref_k[t[b, pos[b] // PS], pos[b] % PS] = kn[b]
+        ref_v[t[b, pos[b] // PS], pos[b] % PS] = vn[b]
+    assert np.array_equal(k2, ref_k.view(np.uint16)) and np.array_equal(v2, ref_v.view(np.uint16))
+    assert err.tolist() == [0, 0, 0, 0]
+    for b in (0, 2, 3):
+        for h in range(Hkv):
+            got = gather(k2.view(np.float16), t, b, pos[b], pos[b] + 1, h)[0]
+            assert np.array_equal(got, kn[b, h].astype(np.float64))
+    changed = np.any(k2 != k.view(np.uint16), axis=(2, 3))
+    assert changed.sum() <= 3  # at most one (page, slot) per sequence with a row
+    # b=1: page id past the pool; b=2: position past its table row (the next
+    # row's first entry, b=3's valid page, must not be written through)
+    bad_pos = np.array([2, 2, 5 * PS, -3], dtype=np.int32)
+    t_bad = t.copy()
+    t_bad[1, 0] = k.shape[0] + 2
+    k3, v3, err = o.kv_append(kn, vn, bad_pos, t_bad, k, v)
+    assert err.tolist() == [0, 1, 1, 0]
+    written = np.any(k3 != k.view(np.uint16), axis=(2, 3))
+    assert written.sum() == 1 and written[t[0, 0], 2]  # only b=0 wrote
+
+
 ALL = [check_half_decoder, check_golden, check_brute_force, check_context_one,
        check_q_zero_mean, check_sharding_identity, check_partial_brute_force, check_window_truncation,
-       check_page_permutation, check_closed_forms, check_invalid_rows]
+       check_page_permutation, check_closed_forms, check_invalid_rows, check_kv_append]
 
 
 def run_all(o):

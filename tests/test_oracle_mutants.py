@@ -30,6 +30,10 @@ MUTANTS = [
     ("merge_ignores_shift", "double c = exp(m[i] - M);", "double c = 1.0;"),
     ("partial_max_unscaled", "if (scale * dot > m) m = scale * dot;", "if (dot > m) m = dot;"),
     ("row_batch_index", "const int b = row / sh->num_q_heads;", "const int b = row % sh->batch;"),
+    ("append_wrong_slot", "(((int64_t)phys * sh->page_size + t % sh->page_size) * sh->num_kv_heads + h) *",
+     "(((int64_t)phys * sh->page_size + (t + 1) % sh->page_size) * sh->num_kv_heads + h) *"),
+    ("append_no_bound_check", "      if (t >= cap) {\n        err = 1;\n      } else {",
+     "      if (0) {\n        err = 1;\n      } else {"),
 ]
 
 
