@@ -159,6 +159,35 @@ int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens, vo
                         void* stream);
 
 /*
+ * Paged K/V append, the step before attention (idle-intelligence/llm-web
+ * pull request 8, suffix-prefill commit: the new K/V rows are scattered into
+ * the cache at their positions after the resident prefix).  For every b with
+ * positions[b] >= 0 and every KV head h:
+ *   k_pages[page_table[b][t / PS]][t % PS][h][:] = k_new[b][h][:],  t = positions[b]
+ * (likewise v).  k_new, v_new: [B][Hkv][D] fp16 device; positions: [B] int32
+ * device.  Uses batch, num_kv_heads, head_dim, page_size, max_pages_per_seq
+ * and num_pages of *p (the other fields must still be valid).  Bit-exact copy.
+ * A position past the table raises DECODE_ATTN_DEV_BAD_LEN, a page id
+ * outside [0, P) DECODE_ATTN_DEV_BAD_PAGE; that sequence is not written.
+ */
+int decode_kv_append(const decode_attn_params* p, const void* k_new, const void* v_new,
+                     const int32_t* positions, void* k_pages, void* v_pages,
+                     const int32_t* page_table, int32_t* err_flag, void* stream);
+
+/*
+ * Append + attention in one launch: the same result as decode_kv_append with
+ * positions[b] = seq_lens[b] - 1 (the new token is the last attended
+ * position; sequences with seq_len 0 get no row) followed by decode_attn.
+ * The CTA holding each sequence's last position writes the new rows of its
+ * KV head before it streams its tiles.  Arguments as decode_attn plus k_new,
+ * v_new ([B][Hkv][D] fp16 device); k_pages and v_pages are written.
+ */
+int decode_attn_append(const decode_attn_params* p, const void* q, const void* k_new,
+                       const void* v_new, void* k_pages, void* v_pages,
+                       const int32_t* page_table, const int32_t* seq_lens, void* out,
+                       void* workspace, size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
  * End-to-end step from HOST buffers: enqueues the host-to-device copies of
  * q, k_pages, v_pages, page_table and seq_lens into the caller's device
  * buffers (d_* arguments, same layouts), decode_attn, and the device-to-host

@@ -26,6 +26,7 @@ __all__ = [
     "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
+    "decode_kv_append", "decode_attn_append",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
@@ -90,6 +91,10 @@ def load_library():
             lib.decode_attn_combine.restype = ctypes.c_int
             lib.decode_attn_host.argtypes = [PP] + [P] * 12 + [sz, P, sz, P, P]
             lib.decode_attn_host.restype = ctypes.c_int
+            lib.decode_kv_append.argtypes = [PP, P, P, P, P, P, P, P, P]
+            lib.decode_kv_append.restype = ctypes.c_int
+            lib.decode_attn_append.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P, P]
+            lib.decode_attn_append.restype = ctypes.c_int
             lib.decode_attn_workspace_clear.argtypes = [PP, P, sz, P]
             lib.decode_attn_workspace_clear.restype = ctypes.c_int
             lib.decode_attn_strerror.argtypes = [ctypes.c_int]
@@ -230,6 +235,54 @@ def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window:
                                     ws_bytes, _ptr(err_flag), _stream_handle(stream))
     if st:
         raise DecodeAttnError(st, "decode_attn")
+    return out
+
+
+def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_flag=None,
+                     stream=None):
+    """Writes the step's new rows k_new/v_new [B,Hkv,D] at positions[b]
+    (int32, -1 = none) into the paged pools, bit for bit."""
+    import torch
+    dev = k_pages.device
+    _check(k_new, torch.float16, "k_new", dev)
+    _check(v_new, torch.float16, "v_new", dev)
+    _check(positions, torch.int32, "positions", dev)
+    _check(k_pages, torch.float16, "k_pages", dev)
+    _check(v_pages, torch.float16, "v_pages", dev)
+    _check(page_table, torch.int32, "page_table", dev)
+    P, PS, Hkv, D = k_pages.shape
+    if tuple(k_new.shape) != (page_table.shape[0], Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [B, Hkv, D]")
+    p = DecodeAttnParams(batch=page_table.shape[0], num_q_heads=Hkv, num_kv_heads=Hkv,
+                         head_dim=D, page_size=PS, max_pages_per_seq=page_table.shape[1],
+                         num_pages=P, max_seq_len=0, scale=1.0, window=0, variant=0,
+                         split_min=0, force_chunk=0)
+    st = load_library().decode_kv_append(ctypes.byref(p), _ptr(k_new), _ptr(v_new),
+                                         _ptr(positions), _ptr(k_pages), _ptr(v_pages),
+                                         _ptr(page_table), _ptr(err_flag),
+                                         _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_kv_append")
+
+
+def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, scale: float,
+                       window: int = 0, out=None, max_seq_len: Optional[int] = None,
+                       workspace=None, err_flag=None, variant: int = VARIANT_AUTO,
+                       split_min: int = 0, force_chunk: int = 0, stream=None):
+    """Append + attention in one launch: writes k_new/v_new [B,Hkv,D] at
+    position seq_lens[b]-1 of each sequence, then attends as decode_attn."""
+    import torch
+    p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
+                                    window, max_seq_len, variant, split_min, force_chunk,
+                                    workspace)
+    _check(k_new, torch.float16, "k_new", q.device)
+    _check(v_new, torch.float16, "v_new", q.device)
+    st = load_library().decode_attn_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                           _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                           _ptr(seq_lens), _ptr(out), _ptr(ws), ws_bytes,
+                                           _ptr(err_flag), _stream_handle(stream))
+    if st:
+        raise DecodeAttnError(st, "decode_attn_append")
     return out
 
 

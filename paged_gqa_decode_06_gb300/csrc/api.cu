@@ -279,7 +279,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? DECODE_ATTN_OK : DECO
 int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const void* q,
               const void* k_pages, const void* v_pages, const int32_t* page_table,
               const int32_t* seq_lens, void* out, const Workspace& ws, int32_t* err_flag,
-              cudaStream_t stream) {
+              cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
   if (p->batch == 0) return DECODE_ATTN_OK;
   SplitLaunch L;
   const int box_t = std::min(p->page_size, kTile);
@@ -297,6 +297,10 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.ws_ml = ws.ml;
   a.counters = ws.counters;
   a.err = err_flag;
+  a.k_new = static_cast<const __half*>(k_new);
+  a.v_new = static_cast<const __half*>(v_new);
+  a.k_pages_w = static_cast<__half*>(const_cast<void*>(k_pages));
+  a.v_pages_w = static_cast<__half*>(const_cast<void*>(v_pages));
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
   a.G = p->num_q_heads / p->num_kv_heads;
@@ -405,6 +409,51 @@ extern "C" int decode_attn(const decode_attn_params* p, const void* q, const voi
   if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
   // the split kernel's last CTA per group merges the partials (no second launch)
   return run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s);
+}
+
+extern "C" int decode_attn_append(const decode_attn_params* p, const void* q, const void* k_new,
+                                  const void* v_new, void* k_pages, void* v_pages,
+                                  const int32_t* page_table, const int32_t* seq_lens, void* out,
+                                  void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                  void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  decode_attn_plan plan;
+  int st = plan_for_stream(p, s, &plan);
+  if (st) return st;
+  if ((st = check_tensors(q, k_pages, v_pages, page_table, seq_lens, out))) return st;
+  if (!k_new || !v_new) return DECODE_ATTN_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return DECODE_ATTN_ERR_ALIGN;
+  Workspace ws;
+  if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
+  return run_split(p, plan, q, k_pages, v_pages, page_table, seq_lens, out, ws, err_flag, s, k_new,
+                   v_new);
+}
+
+extern "C" int decode_kv_append(const decode_attn_params* p, const void* k_new, const void* v_new,
+                                const int32_t* positions, void* k_pages, void* v_pages,
+                                const int32_t* page_table, int32_t* err_flag, void* stream) {
+  int st = check_params(p);
+  if (st) return st;
+  if (!k_new || !v_new || !positions || !k_pages || !v_pages || !page_table)
+    return DECODE_ATTN_ERR_NULL;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+    return DECODE_ATTN_ERR_ALIGN;
+  if (p->batch == 0) return DECODE_ATTN_OK;
+  KvAppendArgs a;
+  a.k_new = static_cast<const uint4*>(k_new);
+  a.v_new = static_cast<const uint4*>(v_new);
+  a.positions = positions;
+  a.page_table = page_table;
+  a.k_pages = static_cast<uint4*>(k_pages);
+  a.v_pages = static_cast<uint4*>(v_pages);
+  a.err = err_flag;
+  a.B = p->batch;
+  a.Hkv = p->num_kv_heads;
+  a.chunks = p->head_dim / 8;
+  a.page_size = p->page_size;
+  a.max_pages = p->max_pages_per_seq;
+  a.num_pages = p->num_pages;
+  return cuda_status(launch_kv_append(a, static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int decode_attn_host(const decode_attn_params* p, const void* q_host,

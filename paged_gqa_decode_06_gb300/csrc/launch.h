@@ -28,6 +28,18 @@ cudaError_t launch_combine_d64(const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_combine_d128(const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_combine_d256(const CombineArgs& a, cudaStream_t stream);
 
+struct KvAppendArgs {
+  const uint4* k_new;   // [B][Hkv][D] as 16-byte chunks
+  const uint4* v_new;
+  const int32_t* positions;
+  const int32_t* page_table;
+  uint4* k_pages;       // [P][PS][Hkv][D] as 16-byte chunks
+  uint4* v_pages;
+  int32_t* err;
+  int32_t B, Hkv, chunks, page_size, max_pages, num_pages;
+};
+cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t stream);
+
 // Resident CTAs per SM the kernels are sized for (shared-memory bound).
 int simt_ctas_per_sm(int head_dim);
 size_t simt_smem_bytes(int head_dim);

@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   const bool bad = bad_s != 0;
 
   if (warp == kWarps) {
+    if (a.k_new != nullptr && s == r.nshards - 1 && !bad) append_new_rows<D>(a, r, b, h, lane);
     if (lane == 0 && !bad) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);

@@ -38,6 +38,10 @@ struct SplitArgs {
   float2* ws_ml;              // [B*Hq*S_max] (m, l) (split; l = -1 marks a bad row)
   int32_t* counters;          // [B*Hkv] shards finished per group (split; zero on entry)
   int32_t* err;               // nullable
+  const __half* k_new;        // [B][Hkv][D] rows to append at seq_len - 1, or null
+  const __half* v_new;
+  __half* k_pages_w;          // the pool, written only when appending
+  __half* v_pages_w;
   int32_t Hq, Hkv, G;
   int32_t max_pages, num_pages, page_size, page_shift, box_tokens;
   int32_t window, chunk, max_shards, split;
@@ -101,6 +105,28 @@ __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h
     const int g = e / D, d = e % D;
     a.out[((size_t)b * a.Hq + h * a.G + g) * D + d] = __float2half_rn(0.f);
   }
+}
+
+// Fused append (producer warp, before any TMA of this CTA): the CTA holding
+// a sequence's last position writes the step's new K/V rows of its head
+// there, then fences the generic-proxy writes against the TMA reads that
+// follow (the rows are read back through L2 like every other row).
+template <int D>
+__device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRange& r, int b,
+                                                int h, int lane) {
+  const int pos = r.end - 1;
+  const int phys = a.page_table[(size_t)b * a.max_pages + (pos >> a.page_shift)];
+  const size_t off =
+      (((size_t)phys * a.page_size + (pos & (a.page_size - 1))) * a.Hkv + h) * D;
+  const size_t src = ((size_t)b * a.Hkv + h) * D;
+  for (int c = lane; c < D / 8; c += 32) {
+    reinterpret_cast<uint4*>(a.k_pages_w + off)[c] =
+        reinterpret_cast<const uint4*>(a.k_new + src)[c];
+    reinterpret_cast<uint4*>(a.v_pages_w + off)[c] =
+        reinterpret_cast<const uint4*>(a.v_new + src)[c];
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
 }
 
 // Split path epilogue, run by the consumer threads [0, nthreads) after this
@@ -219,6 +245,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   const bool bad = bad_s != 0;
 
   if (warp == kWarps) {
+    if (a.k_new != nullptr && s == r.nshards - 1 && !bad) append_new_rows<D>(a, r, b, h, lane);
     if (lane == 0 && !bad) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
