@@ -65,6 +65,9 @@ def _bind(lib):
     lib.oracle_partial_f64.restype = ctypes.c_int
     lib.oracle_merge_f64.argtypes = [i32, i32, P, P, P, P]
     lib.oracle_merge_f64.restype = None
+    lib.oracle_decode_attn_multi_f64.argtypes = [
+        ctypes.POINTER(OracleShape), i32, P, P, P, P, P, f64, i32, P, P]
+    lib.oracle_decode_attn_multi_f64.restype = ctypes.c_int
     lib.oracle_kv_append_u16.argtypes = [ctypes.POINTER(OracleShape), P, P, P, P, P, P, P]
     lib.oracle_kv_append_u16.restype = ctypes.c_int
     return lib
@@ -209,6 +212,29 @@ def _kv_append(lib, k_new, v_new, positions, page_table, k_pages, v_pages):
     return ka, va, err[:B]
 
 
+def _decode_attn_multi(lib, q, k_pages, v_pages, page_table, seq_lens, scale, window=0,
+                       return_errors=False):
+    """Several query positions per sequence: q [B,T,Hq,D] -> out [B,T,Hq,D]
+    f64; query t of sequence b sits at position seq_lens[b] - T + t."""
+    qa = _as_u16(q)
+    B, T, Hq, D = qa.shape
+    ka, va = _as_u16(k_pages), _as_u16(v_pages)
+    pt, sl = _as_i32(page_table), _as_i32(seq_lens)
+    P_, PS, Hkv, _ = ka.shape
+    sh = OracleShape(B, Hq, Hkv, D, PS, pt.shape[1], P_)
+    out = np.zeros((max(B * T * Hq, 1), D), dtype=np.float64)
+    err = np.zeros(max(B * T * Hq, 1), dtype=np.int32)
+    st = lib.oracle_decode_attn_multi_f64(ctypes.byref(sh), T, _ptr(qa), _ptr(ka), _ptr(va),
+                                          _ptr(pt), _ptr(sl), float(scale), int(window),
+                                          _ptr(out), _ptr(err))
+    if st < 0:
+        raise ValueError("oracle: bad shape")
+    out = out[:B * T * Hq].reshape(B, T, Hq, D)
+    if return_errors:
+        return out, err[:B * T * Hq].reshape(B, T, Hq)
+    return out
+
+
 class Oracle:
     """The oracle's entry points bound to one compiled library."""
 
@@ -229,6 +255,9 @@ class Oracle:
 
     def kv_append(self, *a, **k):
         return _kv_append(self.lib, *a, **k)
+
+    def decode_attn_multi(self, *a, **k):
+        return _decode_attn_multi(self.lib, *a, **k)
 
 
 def default() -> Oracle:
@@ -255,3 +284,8 @@ def merge(*a, **k):
 def kv_append(*a, **k):
     """See ``_kv_append``."""
     return _kv_append(_load(), *a, **k)
+
+
+def decode_attn_multi(*a, **k):
+    """See ``_decode_attn_multi``."""
+    return _decode_attn_multi(_load(), *a, **k)

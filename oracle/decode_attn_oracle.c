@@ -346,3 +346,47 @@ int oracle_kv_append_u16(const oracle_shape* sh, const uint16_t* k_new, const ui
   }
   return bad;
 }
+
+/* ---- several new query positions per sequence (causal) ------------------ */
+
+/*
+ * idle-intelligence/llm-web pull request 8, suffix-prefill commit: new tokens
+ * attend to the resident cache and to each other (their K/V already
+ * appended).  With T new tokens per sequence and L = seq_lens[b] counting
+ * them, query t (0 <= t < T) of sequence b sits at position P = L - T + t and
+ * attends the positions [lo, P + 1) with lo = (window > 0) ? max(0, P + 1 -
+ * window) : 0: causal order among the new tokens, the window counted from
+ * each query's own position.  A query with P < 0 (fewer cached positions
+ * than queries) gives a zero row.  q is [B][T][Hq][D], out [B*T*Hq][D] in the
+ * same order.  Each row is the single-query definition above with the
+ * sequence length P + 1.  Returns the number of invalid rows, -1 on a bad
+ * shape.
+ */
+int oracle_decode_attn_multi_f64(const oracle_shape* sh, int32_t T, const uint16_t* q,
+                                 const uint16_t* k_pages, const uint16_t* v_pages,
+                                 const int32_t* page_table, const int32_t* seq_lens,
+                                 double scale, int32_t window, double* out, int32_t* row_err) {
+  if (!shape_ok(sh) || T < 1) return -1;
+  const int D = sh->head_dim;
+  const int64_t cap = (int64_t)sh->max_pages * sh->page_size;
+  int bad = 0;
+  for (int b = 0; b < sh->batch; ++b) {
+    for (int t = 0; t < T; ++t) {
+      /* the sequence as query t sees it: one batch entry of length P + 1 */
+      int64_t L = seq_lens[b];
+      int32_t len_t = (L < 0 || L > cap) ? -1 : (int32_t)(L - T + t + 1);
+      if (len_t < 0 && L >= 0 && L <= cap) len_t = 0;
+      oracle_shape one = *sh;
+      one.batch = 1;
+      for (int hq = 0; hq < sh->num_q_heads; ++hq) {
+        int64_t row = ((int64_t)b * T + t) * sh->num_q_heads + hq;
+        int st = one_row(&one, q + ((int64_t)b * T + t) * sh->num_q_heads * D,
+                         k_pages, v_pages, page_table + (int64_t)b * sh->max_pages, &len_t,
+                         scale, window, hq, out + row * D);
+        if (row_err) row_err[row] = st ? 1 : 0;
+        bad += st ? 1 : 0;
+      }
+    }
+  }
+  return bad;
+}

@@ -305,9 +305,43 @@ def check_kv_append(o):
     assert written.sum() == 1 and written[t[0, 0], 2]  # only b=0 wrote
 
 
+def check_multi_query(o):
+    """T new query positions per sequence: scipy brute force with an explicit
+    causal mask (query t at position L - T + t sees positions up to itself,
+    the window counted from there); each query equals the single-query
+    definition on the sequence cut after its own position; queries before the
+    first cached position give zero rows."""
+    rng = np.random.default_rng(21)
+    lens = [9, 2, 17]
+    T, Hq, Hkv, D, PS = 3, 4, 2, 8, 4
+    _, k, v, t, L = rand_case(rng, 3, Hq, Hkv, D, PS, lens)
+    q = rng.standard_normal((3, T, Hq, D)).astype(np.float16)
+    for window in (0, 4):
+        got = o.decode_attn_multi(q, k, v, t, L, 0.45, window)
+        for b, n in enumerate(lens):
+            for tq in range(T):
+                P = n - T + tq
+                for hq in range(Hq):
+                    if P < 0:
+                        assert not np.any(got[b, tq, hq])
+                        continue
+                    lo = max(0, P + 1 - window) if window > 0 else 0
+                    K = gather(k, t, b, lo, P + 1, hq // 2)
+                    V = gather(v, t, b, lo, P + 1, hq // 2)
+                    w = softmax(0.45 * (K @ q[b, tq, hq].astype(np.float64)))
+                    assert rel_err(got[b, tq, hq], w @ V) <= 1e-12, (window, b, tq, hq)
+            for tq in range(T):
+                cut = np.array([max(0, n - T + tq + 1)], dtype=np.int32)
+                single = o.decode_attn(q[b:b + 1, tq], k, v, t[b:b + 1], cut, 0.45, window)
+                assert np.array_equal(got[b, tq], single[0])
+    one = o.decode_attn_multi(q[:, :1], k, v, t, L - (T - 1), 0.45, 0)
+    assert np.array_equal(one[:, 0], o.decode_attn(q[:, 0], k, v, t, L - (T - 1), 0.45, 0))
+
+
 ALL = [check_half_decoder, check_golden, check_brute_force, check_context_one,
        check_q_zero_mean, check_sharding_identity, check_partial_brute_force, check_window_truncation,
-       check_page_permutation, check_closed_forms, check_invalid_rows, check_kv_append]
+       check_page_permutation, check_closed_forms, check_invalid_rows, check_kv_append,
+       check_multi_query]
 
 
 def run_all(o):

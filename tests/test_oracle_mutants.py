@@ -30,6 +30,10 @@ MUTANTS = [
     ("merge_ignores_shift", "double c = exp(m[i] - M);", "double c = 1.0;"),
     ("partial_max_unscaled", "if (scale * dot > m) m = scale * dot;", "if (dot > m) m = dot;"),
     ("row_batch_index", "const int b = row / sh->num_q_heads;", "const int b = row % sh->batch;"),
+    ("multi_causal_off_by_one", "int32_t len_t = (L < 0 || L > cap) ? -1 : (int32_t)(L - T + t + 1);",
+     "int32_t len_t = (L < 0 || L > cap) ? -1 : (int32_t)(L - T + t);"),
+    ("multi_query_row_stride", "int st = one_row(&one, q + ((int64_t)b * T + t) * sh->num_q_heads * D,",
+     "int st = one_row(&one, q + ((int64_t)t * sh->batch + b) * sh->num_q_heads * D,"),
     ("append_wrong_slot", "(((int64_t)phys * sh->page_size + t % sh->page_size) * sh->num_kv_heads + h) *",
      "(((int64_t)phys * sh->page_size + (t + 1) % sh->page_size) * sh->num_kv_heads + h) *"),
     ("append_no_bound_check", "      if (t >= cap) {\n        err = 1;\n      } else {",
