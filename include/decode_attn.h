@@ -16,13 +16,13 @@
  * split partials merged in a fixed order by a combine kernel).
  *
  * Layouts (all row-major, contiguous, device memory unless stated):
- *   q           [B][Hq][D]              fp16
+ *   q           [B][Hq][D]              fp16   ([B][T][Hq][D] with num_queries T > 1)
  *   k_pages     [P][PS][Hkv][D]         fp16   (the caller's paged cache)
  *   v_pages     [P][PS][Hkv][D]         fp16
  *   page_table  [B][max_pages_per_seq]  int32  (physical page of each logical page)
  *   seq_lens    [B]                     int32  (positions to attend, the new
  *                                                token's K/V already in the cache)
- *   out         [B][Hq][D]              fp16
+ *   out         [B][Hq][D]              fp16   ([B][T][Hq][D] with num_queries T > 1)
  * Ownership: the caller owns every buffer, including the workspace; the
  * library allocates no device memory and keeps no per-call state (only a
  * per-device cache of the SM count).  Entry points are thread-safe.
@@ -87,6 +87,11 @@ typedef struct decode_attn_params {
   int32_t variant;           /* DECODE_ATTN_VARIANT_*; 0 = automatic */
   int32_t split_min;         /* contexts above this use shards + combine; <= 0 means 256 */
   int32_t force_chunk;       /* > 0: tokens per shard (rounded up to 64); 0 = planner */
+  int32_t num_queries;       /* T new query positions per sequence (<= 0 means 1); with
+                                T > 1, q and out are [B][T][Hq][D], query t of sequence b
+                                sits at position seq_lens[b] - T + t and attends causally
+                                (up to itself; the window counted from it); needs
+                                T * G <= 16 and the tensor-core variant */
 } decode_attn_params;
 
 /* Launch plan chosen by the host heuristic (exposed for inspection/tests). */

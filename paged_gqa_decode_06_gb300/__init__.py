@@ -44,7 +44,8 @@ class DecodeAttnParams(ctypes.Structure):
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "page_size",
         "max_pages_per_seq", "num_pages", "max_seq_len")] + [
         ("scale", ctypes.c_float), ("window", ctypes.c_int32), ("variant", ctypes.c_int32),
-        ("split_min", ctypes.c_int32), ("force_chunk", ctypes.c_int32)]
+        ("split_min", ctypes.c_int32), ("force_chunk", ctypes.c_int32),
+        ("num_queries", ctypes.c_int32)]
 
 
 class DecodeAttnPlan(ctypes.Structure):
@@ -110,10 +111,14 @@ def decode_attn_strerror(code: int) -> str:
 def make_params(q, k_pages, page_table, scale: float, window: int = 0,
                 max_seq_len: Optional[int] = None, variant: int = VARIANT_AUTO,
                 split_min: int = 0, force_chunk: int = 0) -> DecodeAttnParams:
-    """Parameters from tensor shapes: q [B,Hq,D], k_pages [P,PS,Hkv,D],
-    page_table [B,maxPages].  ``max_seq_len`` is a host-side bound on
-    seq_lens (it sizes the grid; None = the page table's capacity)."""
-    B, Hq, D = q.shape
+    """Parameters from tensor shapes: q [B,Hq,D] (or [B,T,Hq,D] for T query
+    positions per sequence), k_pages [P,PS,Hkv,D], page_table [B,maxPages].
+    ``max_seq_len`` is a host-side bound on seq_lens (it sizes the grid;
+    None = the page table's capacity)."""
+    if len(q.shape) == 4:
+        B, T, Hq, D = q.shape
+    else:
+        (B, Hq, D), T = q.shape, 1
     P, PS, Hkv, D2 = k_pages.shape
     if D2 != D:
         raise ValueError("q and k_pages head_dim differ")
@@ -122,7 +127,7 @@ def make_params(q, k_pages, page_table, scale: float, window: int = 0,
         max_pages_per_seq=page_table.shape[1], num_pages=P,
         max_seq_len=int(max_seq_len) if max_seq_len else 0, scale=float(scale),
         window=int(window), variant=int(variant), split_min=int(split_min),
-        force_chunk=int(force_chunk))
+        force_chunk=int(force_chunk), num_queries=int(T))
 
 
 def decode_attn_make_plan(params: DecodeAttnParams, num_sms: int) -> DecodeAttnPlan:
@@ -256,7 +261,7 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
     p = DecodeAttnParams(batch=page_table.shape[0], num_q_heads=Hkv, num_kv_heads=Hkv,
                          head_dim=D, page_size=PS, max_pages_per_seq=page_table.shape[1],
                          num_pages=P, max_seq_len=0, scale=1.0, window=0, variant=0,
-                         split_min=0, force_chunk=0)
+                         split_min=0, force_chunk=0, num_queries=1)
     st = load_library().decode_kv_append(ctypes.byref(p), _ptr(k_new), _ptr(v_new),
                                          _ptr(positions), _ptr(k_pages), _ptr(v_pages),
                                          _ptr(page_table), _ptr(err_flag),
@@ -269,8 +274,9 @@ def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, 
                        window: int = 0, out=None, max_seq_len: Optional[int] = None,
                        workspace=None, err_flag=None, variant: int = VARIANT_AUTO,
                        split_min: int = 0, force_chunk: int = 0, stream=None):
-    """Append + attention in one launch: writes k_new/v_new [B,Hkv,D] at
-    position seq_lens[b]-1 of each sequence, then attends as decode_attn."""
+    """Append + attention in one launch: writes k_new/v_new [B,Hkv,D] (or
+    [B,T,Hkv,D] with q [B,T,Hq,D]) at the last T positions of each sequence
+    (seq_lens counts them), then attends as decode_attn."""
     import torch
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,

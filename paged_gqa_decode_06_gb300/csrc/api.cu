@@ -59,7 +59,7 @@ int check_params(const decode_attn_params* p) {
       (int64_t)p->num_pages * p->page_size >= INT32_MAX)
     return DECODE_ATTN_ERR_SHAPE;
   if (p->num_q_heads / p->num_kv_heads > 16) return DECODE_ATTN_ERR_GROUP;
-  if (!std::isfinite(p->scale)) return DECODE_ATTN_ERR_SHAPE;
+  if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -72,6 +72,8 @@ size_t ticket_region_bytes(const decode_attn_params* p) {
   const size_t need = ((size_t)p->batch * p->num_kv_heads * 4 + 255) / 256 * 256;
   return need > kTicketRegion ? need : kTicketRegion;
 }
+
+int num_queries(const decode_attn_params* p) { return p->num_queries > 1 ? p->num_queries : 1; }
 
 int next_pow2(int x) {
   int r = 1;
@@ -105,15 +107,18 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   std::memset(plan, 0, sizeof(*plan));
   const int G = p->num_q_heads / p->num_kv_heads;
   const int gp = next_pow2(G);
+  const int T = p->num_queries > 1 ? p->num_queries : 1;
   int variant = p->variant;
   // the tensor-core variant measured faster on every shape (G = 4 and 8,
   // D = 64..256); the CUDA-core variant stays selectable
   if (variant == DECODE_ATTN_VARIANT_AUTO) variant = DECODE_ATTN_VARIANT_MMA;
   int group_pad = gp;
   if (variant == DECODE_ATTN_VARIANT_SIMT) {
-    if (gp > 8) return DECODE_ATTN_ERR_VARIANT;
+    if (gp > 8 || T > 1) return DECODE_ATTN_ERR_VARIANT;
   } else if (variant == DECODE_ATTN_VARIANT_MMA) {
-    group_pad = gp <= 8 ? 8 : 16;  // one or two n8 tiles of heads
+    const int rows = T * G;  // query rows per KV head: one or two n8 tiles
+    if (rows > 16) return DECODE_ATTN_ERR_VARIANT;
+    group_pad = rows <= 8 ? 8 : 16;
   } else {
     return DECODE_ATTN_ERR_VARIANT;
   }
@@ -121,7 +126,9 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   const int64_t capacity = (int64_t)p->max_pages_per_seq * p->page_size;
   const int64_t max_len =
       p->max_seq_len > 0 ? std::min<int64_t>(p->max_seq_len, capacity) : capacity;
-  const int64_t attended = p->window > 0 ? std::min<int64_t>(max_len, p->window) : max_len;
+  // T queries: the first one's window starts T - 1 positions earlier
+  const int64_t attended =
+      p->window > 0 ? std::min<int64_t>(max_len, (int64_t)p->window + T - 1) : max_len;
   // positions from the tile-aligned base to the end of the longest sequence
   const int64_t span = std::max<int64_t>(1, p->window > 0 ? attended + kTile - 1 : max_len);
   const int box_t = std::min(p->page_size, kTile);
@@ -174,7 +181,7 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->ctas_per_sm = ctas_per_sm;
   if (plan->split) {
     // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
-    const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)max_shards;
+    const size_t rows = (size_t)p->batch * T * p->num_q_heads * (size_t)max_shards;
     plan->workspace_bytes = ticket_region_bytes(p) + round_up(rows * sizeof(float2), 256) +
                             round_up(rows * p->head_dim * 4, 256);
   }
@@ -263,7 +270,7 @@ int workspace_views(const decode_attn_params* p, const decode_attn_plan& plan, v
   if (!plan.split) return DECODE_ATTN_OK;
   if (!ws || ws_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
     return DECODE_ATTN_ERR_WORKSPACE;
-  const size_t rows = (size_t)p->batch * p->num_q_heads * (size_t)plan.max_shards;
+  const size_t rows = (size_t)p->batch * num_queries(p) * p->num_q_heads * (size_t)plan.max_shards;
   char* base = static_cast<char*>(ws);
   const size_t tickets = ticket_region_bytes(p);
   const size_t ml_bytes = round_up(rows * sizeof(float2), 256);
@@ -313,6 +320,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.chunk = plan.chunk_tokens;
   a.max_shards = plan.max_shards;
   a.split = plan.split;
+  a.T = num_queries(p);
   a.scale_log2 = p->scale * kLog2e;
   L.grid = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
   L.group_pad = plan.group_pad;
@@ -338,6 +346,7 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
   a.B = p->batch;
   a.Hq = p->num_q_heads;
   a.G = p->num_q_heads / p->num_kv_heads;
+  a.T = num_queries(p);
   a.capacity = p->max_pages_per_seq * p->page_size;
   a.window = p->window > 0 ? p->window : 0;
   a.chunk = plan.chunk_tokens;
@@ -471,7 +480,7 @@ extern "C" int decode_attn_host(const decode_attn_params* p, const void* q_host,
   if ((st = check_tensors(d_q, d_k_pages, d_v_pages, d_page_table, d_seq_lens, d_out))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t D = p->head_dim;
-  const size_t q_bytes = (size_t)p->batch * p->num_q_heads * D * 2;
+  const size_t q_bytes = (size_t)p->batch * num_queries(p) * p->num_q_heads * D * 2;
   const size_t pool = (size_t)p->num_pages * p->page_size * p->num_kv_heads * D * 2;
   const size_t kv = (kv_bytes_to_copy == 0 || kv_bytes_to_copy > pool) ? pool : kv_bytes_to_copy;
   const size_t pt_bytes = (size_t)p->batch * p->max_pages_per_seq * 4;

@@ -20,11 +20,17 @@ namespace pgd {
 
 struct CombineArgs {
   const int32_t* seq_lens;
-  const float* ws_acc;   // [B*Hq*S_max][D]
-  const float2* ws_ml;   // [B*Hq*S_max]
-  __half* out;           // [B][Hq][D]
-  int32_t B, Hq, G, capacity, window, chunk, max_shards;
+  const float* ws_acc;   // [B*T*Hq*S_max][D]
+  const float2* ws_ml;   // [B*T*Hq*S_max]
+  __half* out;           // [B][T][Hq][D]
+  int32_t B, Hq, G, T, capacity, window, chunk, max_shards;
 };
+
+// Output row of the group's r-th query row (r = t * G + g): query t of
+// sequence b, query head h * G + g.
+__device__ __forceinline__ size_t group_row(int b, int h, int r, int T, int G, int Hq) {
+  return ((size_t)b * T + r / G) * Hq + (size_t)h * G + r % G;
+}
 
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -42,7 +48,7 @@ __host__ __device__ constexpr int merge_smem_bytes(int G) {
   return G * kShardBlock * 8 + kMaxMergeRows * 8;
 }
 
-// Merges the S shards of group (b, h) into out, using threads [0, nthreads)
+// Merges the S shards of group (b, h) (its T*G query rows) into out, using threads [0, nthreads)
 // (tid = this thread's index among them) and `smem` (merge_smem_bytes(G)
 // bytes, 16-byte aligned).  `sync` is a barrier over exactly those threads.
 // dead forces zero rows (an invalid range).
@@ -50,11 +56,10 @@ template <int D, class Sync>
 __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, int S, bool dead,
                                             int tid, int nthreads, uint8_t* smem, Sync sync) {
   constexpr int kQuads = D / 4;
-  const int G = a.G;
+  const int G = a.T * a.G;  // rows of the group
   float2* ml_s = reinterpret_cast<float2*>(smem);                       // [G][kShardBlock]
   float* max_s = reinterpret_cast<float*>(smem + G * kShardBlock * 8);  // [G]
   int* zero_s = reinterpret_cast<int*>(max_s + kMaxMergeRows);          // [G]
-  const size_t row0 = (size_t)b * a.Hq + (size_t)h * G;
 
   // per-row maximum and bad-partial flag, from (m, l) staged block by block
   sync();
@@ -67,7 +72,8 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     sync();
     for (int e = tid; e < G * n; e += nthreads) {
       const int g = e / n, j = e % n;
-      ml_s[g * kShardBlock + j] = __ldcg(a.ws_ml + (row0 + g) * a.max_shards + s0 + j);
+      ml_s[g * kShardBlock + j] =
+          __ldcg(a.ws_ml + group_row(b, h, g, a.T, a.G, a.Hq) * a.max_shards + s0 + j);
     }
     sync();
     if (tid < G) {
@@ -103,9 +109,11 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     for (int k = 0; k < 2; ++k) {
       const int g = e[k] / kQuads;
       quad[k] = e[k] % kQuads;
-      row[k] = row0 + g;
+      row[k] = group_row(b, h, g, a.T, a.G, a.Hq);
       M[k] = max_s[g];
-      zero[k] = zero_s[g] != 0;
+      // a row with no attended position in any shard (a query before the
+      // first cached position) stays zero
+      zero[k] = zero_s[g] != 0 || M[k] == -INFINITY;
       // (m, l) from shared memory when one block holds them all
       ml[k] = staged ? ml_s + g * kShardBlock : a.ws_ml + row[k] * a.max_shards;
       acc[k] = reinterpret_cast<const float4*>(a.ws_acc + row[k] * a.max_shards * D) + quad[k];
@@ -170,7 +178,8 @@ template <int D>
 __global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(16) uint8_t merge_smem[];
   const int h = blockIdx.x, b = blockIdx.y;
-  const SeqRange r = seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards);
+  const SeqRange r =
+      seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T);
   grid_dependency_wait();
   merge_group<D>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
                  [] { __syncthreads(); });

@@ -115,15 +115,18 @@ struct SeqRange {
   int32_t status;   // 0 or DECODE_ATTN_DEV_* bits
 };
 
+// With T query positions per sequence (the last T positions), the range is
+// the union of the queries' ranges: the first query's window start to L.
 __device__ __forceinline__ SeqRange seq_range(int32_t L, int32_t window, int32_t capacity,
-                                              int32_t chunk, int32_t max_shards) {
+                                              int32_t chunk, int32_t max_shards, int32_t T = 1) {
   SeqRange r{0, 0, 0, 0, 0};
   if (L < 0 || L > capacity) {
     r.status = DECODE_ATTN_DEV_BAD_LEN;
     return r;
   }
   r.end = L;
-  r.start = (window > 0 && L > window) ? L - window : 0;
+  const int32_t first_end = L - T + 1;  // one past the first query's position
+  r.start = (window > 0 && first_end > window) ? first_end - window : 0;
   r.base = r.start & ~(kTile - 1);
   r.nshards = (L > r.start) ? (L - r.base + chunk - 1) / chunk : 0;
   if (r.nshards > max_shards) {

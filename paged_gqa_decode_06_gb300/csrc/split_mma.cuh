@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
-                               a.max_shards);
+                               a.max_shards, a.T);
   if (r.status != 0 || s >= r.nshards) {
     if (s == 0) {
       if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
@@ -147,7 +147,11 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   const bool bad = bad_s != 0;
 
   if (warp == kWarps) {
-    if (a.k_new != nullptr && s == r.nshards - 1 && !bad) append_new_rows<D>(a, r, b, h, lane);
+    if (a.k_new != nullptr && !bad) {
+      const int shard_lo_w = r.base + s * a.chunk;
+      if (r.end - a.T < shard_lo_w + a.chunk && r.end > shard_lo_w)
+        append_new_rows<D>(a, r, b, h, shard_lo_w, lane);
+    }
     if (lane == 0 && !bad) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
@@ -187,14 +191,15 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   const int G = a.G;
   const int gid = lane >> 2, tig = lane & 3;
   // Q^T operand fragments, held for the whole shard
+  const int R = a.T * G;  // query rows of the group: r = t * G + g
   uint32_t qf[NT8][KS][2];
 #pragma unroll
   for (int j = 0; j < NT8; ++j) {
-    const int head = 8 * j + gid;
-    const __half* qrow = a.q + ((size_t)b * a.Hq + h * G + head) * D;
+    const int rr = 8 * j + gid;
+    const __half* qrow = a.q + group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      if (head < G) {
+      if (rr < R) {
         qf[j][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
         qf[j][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig);
       } else {
@@ -209,6 +214,18 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     for (int j = 0; j < NT8; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
+  // attended range of each of this lane's score columns (query rows
+  // 8j + 2*tig + e): causal up to the row's own position, window from there
+  int col_lo[NT8][2], col_hi[NT8][2];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int rr = 8 * j + 2 * tig + e;
+      const int t = rr < R ? rr / G : a.T - 1;
+      col_hi[j][e] = r.end - a.T + t + 1;
+      col_lo[j][e] = a.window > 0 ? max(0, col_hi[j][e] - a.window) : 0;
+    }
   float m_run[NT8][2], l_part[NT8][2];
 #pragma unroll
   for (int j = 0; j < NT8; ++j) {
@@ -262,8 +279,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
         for (int j = 0; j < NT8; ++j) mma_f16_16816(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
       }
       // online softmax over this block's 16 positions
-      const bool ok_a = (tok0 + gid >= lo) && (tok0 + gid < hi);
-      const bool ok_b = (tok0 + gid + 8 >= lo) && (tok0 + gid + 8 < hi);
+      const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
       uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
       bool rescale = false;
       float alpha[NT8][2];
@@ -272,7 +288,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
         float p[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const bool ok = (e < 2) ? ok_a : ok_b;
+          const int tok = (e < 2) ? tok_a : tok_b;
+          const bool ok = tok >= col_lo[j][e & 1] && tok < col_hi[j][e & 1];
           sc[j][e] = ok ? sc[j][e] * a.scale_log2 : -INFINITY;
         }
 #pragma unroll
@@ -362,7 +379,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   named_barrier_sync(1, kWarps * 32);
   const bool dead = bad || abort_s != 0;
 
-  for (int e = threadIdx.x; e < G * D; e += kWarps * 32) {
+  for (int e = threadIdx.x; e < R * D; e += kWarps * 32) {
     const int g = e / D, d = e % D;
     float M = -INFINITY;
 #pragma unroll
@@ -376,7 +393,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       L += c * ml.y;
       O += c * acc_s[(w * GP + g) * D + d];
     }
-    const size_t row = (size_t)b * a.Hq + h * G + g;
+    const size_t row = group_row(b, h, g, a.T, G, a.Hq);
     if (!a.split) {
       a.out[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
     } else {

@@ -45,6 +45,7 @@ struct SplitArgs {
   int32_t Hq, Hkv, G;
   int32_t max_pages, num_pages, page_size, page_shift, box_tokens;
   int32_t window, chunk, max_shards, split;
+  int32_t T;                  // query positions per sequence (1 for the CUDA-core variant)
   float scale_log2;           // scale * log2(e)
 };
 
@@ -101,9 +102,9 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 
 template <int D, int GP>
 __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h) {
-  for (int e = threadIdx.x; e < a.G * D; e += blockDim.x) {
+  for (int e = threadIdx.x; e < a.T * a.G * D; e += blockDim.x) {
     const int g = e / D, d = e % D;
-    a.out[((size_t)b * a.Hq + h * a.G + g) * D + d] = __float2half_rn(0.f);
+    a.out[group_row(b, h, g, a.T, a.G, a.Hq) * D + d] = __float2half_rn(0.f);
   }
 }
 
@@ -113,17 +114,20 @@ __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h
 // follow (the rows are read back through L2 like every other row).
 template <int D>
 __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRange& r, int b,
-                                                int h, int lane) {
-  const int pos = r.end - 1;
-  const int phys = a.page_table[(size_t)b * a.max_pages + (pos >> a.page_shift)];
-  const size_t off =
-      (((size_t)phys * a.page_size + (pos & (a.page_size - 1))) * a.Hkv + h) * D;
-  const size_t src = ((size_t)b * a.Hkv + h) * D;
-  for (int c = lane; c < D / 8; c += 32) {
-    reinterpret_cast<uint4*>(a.k_pages_w + off)[c] =
-        reinterpret_cast<const uint4*>(a.k_new + src)[c];
-    reinterpret_cast<uint4*>(a.v_pages_w + off)[c] =
-        reinterpret_cast<const uint4*>(a.v_new + src)[c];
+                                                int h, int shard_lo, int lane) {
+  for (int i = 0; i < a.T; ++i) {
+    const int pos = r.end - a.T + i;  // position of the i-th new token
+    if (pos < shard_lo || pos >= shard_lo + a.chunk || pos < 0) continue;
+    const int phys = a.page_table[(size_t)b * a.max_pages + (pos >> a.page_shift)];
+    const size_t off =
+        (((size_t)phys * a.page_size + (pos & (a.page_size - 1))) * a.Hkv + h) * D;
+    const size_t src = (((size_t)b * a.T + i) * a.Hkv + h) * D;
+    for (int c = lane; c < D / 8; c += 32) {
+      reinterpret_cast<uint4*>(a.k_pages_w + off)[c] =
+          reinterpret_cast<const uint4*>(a.k_new + src)[c];
+      reinterpret_cast<uint4*>(a.v_pages_w + off)[c] =
+          reinterpret_cast<const uint4*>(a.v_new + src)[c];
+    }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
   __syncwarp();
@@ -156,6 +160,7 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   c.B = 0;
   c.Hq = a.Hq;
   c.G = a.G;
+  c.T = a.T;
   c.capacity = a.max_pages * a.page_size;
   c.window = a.window;
   c.chunk = a.chunk;
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
-                               a.max_shards);
+                               a.max_shards, a.T);
   if (r.status != 0 || s >= r.nshards) {
     // nothing to stream: report a bad length once; shard 0 owns the group's
     // output rows (zero for an empty or invalid range)
@@ -245,7 +250,11 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   const bool bad = bad_s != 0;
 
   if (warp == kWarps) {
-    if (a.k_new != nullptr && s == r.nshards - 1 && !bad) append_new_rows<D>(a, r, b, h, lane);
+    if (a.k_new != nullptr && !bad) {
+      const int shard_lo_w = r.base + s * a.chunk;
+      if (r.end - a.T < shard_lo_w + a.chunk && r.end > shard_lo_w)
+        append_new_rows<D>(a, r, b, h, shard_lo_w, lane);
+    }
     if (lane == 0 && !bad) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);

@@ -55,7 +55,7 @@ def test_library_needs_no_driver_at_load(pkg):
 def params(pkg, **kw):
     base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                 max_pages_per_seq=192, num_pages=256, max_seq_len=3060, scale=0.088,
-                window=0, variant=0, split_min=0, force_chunk=0)
+                window=0, variant=0, split_min=0, force_chunk=0, num_queries=1)
     base.update(kw)
     return pkg.DecodeAttnParams(**base)
 
@@ -213,3 +213,23 @@ def test_variant_selection(pkg):
     # automatic choice is a pure function of the shape
     a = pkg.decode_attn_make_plan(params(pkg), 152).variant
     assert a in (1, 2) and a == pkg.decode_attn_make_plan(params(pkg), 152).variant
+
+
+def test_multi_query_plans(pkg):
+    # T query positions per sequence: T * G rows per KV head on the mma side
+    plan = pkg.decode_attn_make_plan(params(pkg, num_queries=2), 152)  # G=4 -> 8 rows
+    assert plan.variant == 2 and plan.group_pad == 8
+    plan = pkg.decode_attn_make_plan(params(pkg, num_queries=4), 152)  # 16 rows
+    assert plan.group_pad == 16
+    for bad in (dict(num_queries=5), dict(num_queries=2, variant=1)):
+        with pytest.raises(pkg.DecodeAttnError) as e:
+            pkg.decode_attn_make_plan(params(pkg, **bad), 152)
+        assert e.value.code == -10
+    # the window of the first query starts T - 1 positions earlier
+    p = params(pkg, batch=1, max_pages_per_seq=2048, num_pages=4096, max_seq_len=30000,
+               window=1000, num_queries=4)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    assert plan.chunk_tokens * plan.max_shards >= 1000 + 3 + 63
+    one = pkg.decode_attn_make_plan(params(pkg, num_queries=1), 152)
+    four = pkg.decode_attn_make_plan(params(pkg, num_queries=4), 152)
+    assert four.workspace_bytes - 65536 >= 4 * (one.workspace_bytes - 65536) - 4096
