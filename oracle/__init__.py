@@ -35,6 +35,7 @@ class OracleShape(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("max_pages", ctypes.c_int32),
         ("num_pages", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
     ]
 
 
@@ -57,6 +58,8 @@ def _bind(lib):
     i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
     lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_half_to_double.restype = f64
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = f64
     lib.oracle_decode_attn_f64.argtypes = [
         ctypes.POINTER(OracleShape), P, P, P, P, P, f64, i32, P, i32, i32, P, P]
     lib.oracle_decode_attn_f64.restype = ctypes.c_int
@@ -102,12 +105,32 @@ def _ptr(a: np.ndarray):
     return ctypes.c_void_p(a.ctypes.data)
 
 
+class Bf16(np.ndarray):
+    """uint16 array marked as holding bfloat16 bit patterns."""
+
+
+def as_bf16_bits(a) -> "Bf16":
+    return np.ascontiguousarray(a, dtype=np.uint16).view(Bf16)
+
+
+def dtype_code(x) -> int:
+    """0 for fp16 data, 1 for bfloat16 (torch.bfloat16 tensors or Bf16 arrays)."""
+    if isinstance(x, Bf16):
+        return 1
+    if hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        return 1
+    return 0
+
+
 def _as_u16(x) -> np.ndarray:
-    """fp16 data (numpy float16/uint16 or a CPU torch.float16 tensor) as uint16."""
+    """16-bit float data (numpy float16/uint16, or a CPU torch.float16 /
+    torch.bfloat16 tensor) as its uint16 bit patterns."""
     if hasattr(x, "detach"):  # torch tensor
         import torch
         x = x.detach().to("cpu").contiguous().view(torch.int16).numpy()
     a = np.ascontiguousarray(x)
+    if isinstance(a, Bf16):
+        a = a.view(np.ndarray)
     if a.dtype == np.float16 or a.dtype == np.int16:
         a = a.view(np.uint16)
     assert a.dtype == np.uint16, a.dtype
@@ -124,11 +147,15 @@ def shape_of(q, k_pages, page_table) -> OracleShape:
     B, Hq, D = q.shape
     P, PS, Hkv, D2 = k_pages.shape
     assert D == D2
-    return OracleShape(B, Hq, Hkv, D, PS, page_table.shape[1], P)
+    return OracleShape(B, Hq, Hkv, D, PS, page_table.shape[1], P, dtype_code(k_pages))
 
 
 def _half_to_double(lib, bits: int) -> float:
     return lib.oracle_half_to_double(bits)
+
+
+def _bf16_to_double(lib, bits: int) -> float:
+    return lib.oracle_bf16_to_double(bits)
 
 
 def default_threads() -> int:
@@ -221,7 +248,7 @@ def _decode_attn_multi(lib, q, k_pages, v_pages, page_table, seq_lens, scale, wi
     ka, va = _as_u16(k_pages), _as_u16(v_pages)
     pt, sl = _as_i32(page_table), _as_i32(seq_lens)
     P_, PS, Hkv, _ = ka.shape
-    sh = OracleShape(B, Hq, Hkv, D, PS, pt.shape[1], P_)
+    sh = OracleShape(B, Hq, Hkv, D, PS, pt.shape[1], P_, dtype_code(k_pages))
     out = np.zeros((max(B * T * Hq, 1), D), dtype=np.float64)
     err = np.zeros(max(B * T * Hq, 1), dtype=np.int32)
     st = lib.oracle_decode_attn_multi_f64(ctypes.byref(sh), T, _ptr(qa), _ptr(ka), _ptr(va),
@@ -243,6 +270,9 @@ class Oracle:
 
     def half_to_double(self, bits):
         return _half_to_double(self.lib, bits)
+
+    def bf16_to_double(self, bits):
+        return _bf16_to_double(self.lib, bits)
 
     def decode_attn(self, *a, **k):
         return _decode_attn(self.lib, *a, **k)

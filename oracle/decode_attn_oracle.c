@@ -51,6 +51,7 @@ typedef struct {
   int32_t page_size;       /* PS */
   int32_t max_pages;       /* columns of page_table */
   int32_t num_pages;       /* P, rows of k_pages / v_pages */
+  int32_t dtype;           /* element format of q, K, V: 0 = IEEE binary16, 1 = bfloat16 */
 } oracle_shape;
 
 /* ---- IEEE 754 binary16 -> binary64, from the format's definition ------- */
@@ -74,14 +75,39 @@ double oracle_half_to_double(uint16_t bits) {
   return s ? -mag : mag;
 }
 
+/* bfloat16 -> binary64: the upper half of an IEEE binary32, i.e. sign (1
+ * bit), biased exponent e (8 bits, bias 127), fraction f (7 bits):
+ *   e == 0:         (-1)^s * 2^-126 * (f / 128)        (zero / subnormal)
+ *   0 < e < 255:    (-1)^s * 2^(e-127) * (1 + f / 128)
+ *   e == 255:       infinity (f == 0) or NaN           */
+double oracle_bf16_to_double(uint16_t bits) {
+  int s = (bits >> 15) & 1;
+  int e = (bits >> 7) & 0xff;
+  int f = bits & 0x7f;
+  double mag;
+  if (e == 0) {
+    mag = ldexp((double)f, -133);
+  } else if (e == 255) {
+    mag = (f == 0) ? INFINITY : NAN;
+  } else {
+    mag = ldexp(128.0 + (double)f, e - 134);
+  }
+  return s ? -mag : mag;
+}
+
 static double g_half_table[65536];
+static double g_bf16_table[65536];
 static pthread_once_t g_half_once = PTHREAD_ONCE_INIT;
 static void build_half_table(void) {
-  for (uint32_t i = 0; i < 65536u; ++i) g_half_table[i] = oracle_half_to_double((uint16_t)i);
+  for (uint32_t i = 0; i < 65536u; ++i) {
+    g_half_table[i] = oracle_half_to_double((uint16_t)i);
+    g_bf16_table[i] = oracle_bf16_to_double((uint16_t)i);
+  }
 }
-static const double* half_table(void) {
+/* decoding table of the shape's element format */
+static const double* elem_table(const oracle_shape* sh) {
   pthread_once(&g_half_once, build_half_table);
-  return g_half_table;
+  return sh->dtype == 1 ? g_bf16_table : g_half_table;
 }
 
 /* ---- gather through the page table ------------------------------------- */
@@ -116,7 +142,7 @@ static int attended_range(const oracle_shape* sh, const int32_t* seq_lens, int b
 static int one_row(const oracle_shape* sh, const uint16_t* q, const uint16_t* k_pages,
                    const uint16_t* v_pages, const int32_t* page_table, const int32_t* seq_lens,
                    double scale, int32_t window, int32_t row, double* out) {
-  const double* H = half_table();
+  const double* H = elem_table(sh);
   const int D = sh->head_dim;
   const int G = sh->num_q_heads / sh->num_kv_heads;
   const int b = row / sh->num_q_heads;
@@ -183,7 +209,7 @@ static void* run_rows(void* arg) {
 static int shape_ok(const oracle_shape* sh) {
   return sh && sh->batch >= 0 && sh->num_q_heads > 0 && sh->num_kv_heads > 0 &&
          sh->num_q_heads % sh->num_kv_heads == 0 && sh->head_dim > 0 && sh->page_size > 0 &&
-         sh->max_pages >= 0 && sh->num_pages >= 0;
+         sh->max_pages >= 0 && sh->num_pages >= 0 && (sh->dtype == 0 || sh->dtype == 1);
 }
 
 /*
@@ -238,7 +264,7 @@ int oracle_partial_f64(const oracle_shape* sh, const uint16_t* q, const uint16_t
                        double scale, int64_t lo, int64_t hi, double* m_out, double* l_out,
                        double* acc) {
   if (!shape_ok(sh)) return -1;
-  const double* H = half_table();
+  const double* H = elem_table(sh);
   const int D = sh->head_dim;
   const int h = hq / (sh->num_q_heads / sh->num_kv_heads);
   const uint16_t* qrow = q + ((int64_t)b * sh->num_q_heads + hq) * D;

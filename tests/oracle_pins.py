@@ -338,10 +338,42 @@ def check_multi_query(o):
     assert np.array_equal(one[:, 0], o.decode_attn(q[:, 0], k, v, t, L - (T - 1), 0.45, 0))
 
 
+def bf16_bits_to_f64(bits):
+    """bfloat16 is the upper half of an IEEE binary32: decode through numpy's
+    float32."""
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_bf16(o):
+    """bfloat16 elements: the decoder on all 65536 codes, then scipy brute
+    force on bf16 q/K/V, and a one-position context returns the V row."""
+    import oracle
+    codes = np.arange(65536, dtype=np.uint32)
+    ref = bf16_bits_to_f64(codes)
+    got = np.array([o.bf16_to_double(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+    rng = np.random.default_rng(22)
+    lens = [19, 1, 40]
+    qf, kf, vf, t, L = rand_case(rng, 3, 8, 2, 16, 8, lens)
+    to_bits = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    qb, kb, vb = to_bits(qf), to_bits(kf), to_bits(vf)
+    got = o.decode_attn(oracle.as_bf16_bits(qb), oracle.as_bf16_bits(kb),
+                        oracle.as_bf16_bits(vb), t, L, 0.3, 0)
+    qd, kd, vd = bf16_bits_to_f64(qb), bf16_bits_to_f64(kb), bf16_bits_to_f64(vb)
+    for b, n in enumerate(lens):
+        for hq in range(8):
+            K, V = gather(kd, t, b, 0, n, hq // 4), gather(vd, t, b, 0, n, hq // 4)
+            w = softmax(0.3 * (K @ qd[b, hq]))
+            assert rel_err(got[b, hq], w @ V) <= 1e-12
+    for hq in range(8):  # lens[1] == 1
+        assert np.array_equal(got[1, hq], gather(vd, t, 1, 0, 1, hq // 4)[0])
+
+
 ALL = [check_half_decoder, check_golden, check_brute_force, check_context_one,
        check_q_zero_mean, check_sharding_identity, check_partial_brute_force, check_window_truncation,
        check_page_permutation, check_closed_forms, check_invalid_rows, check_kv_append,
-       check_multi_query]
+       check_multi_query, check_bf16]
 
 
 def run_all(o):

@@ -34,6 +34,8 @@ MUTANTS = [
      "int32_t len_t = (L < 0 || L > cap) ? -1 : (int32_t)(L - T + t);"),
     ("multi_query_row_stride", "int st = one_row(&one, q + ((int64_t)b * T + t) * sh->num_q_heads * D,",
      "int st = one_row(&one, q + ((int64_t)t * sh->batch + b) * sh->num_q_heads * D,"),
+    ("bf16_exponent_bias", "mag = ldexp(128.0 + (double)f, e - 134);",
+     "mag = ldexp(128.0 + (double)f, e - 135);"),
     ("append_wrong_slot", "(((int64_t)phys * sh->page_size + t % sh->page_size) * sh->num_kv_heads + h) *",
      "(((int64_t)phys * sh->page_size + (t + 1) % sh->page_size) * sh->num_kv_heads + h) *"),
     ("append_no_bound_check", "      if (t >= cap) {\n        err = 1;\n      } else {",
