@@ -15,7 +15,8 @@
  * attention" (one K/V row read serves every query head of its GQA group;
  * split partials merged in a fixed order by a combine kernel).
  *
- * Layouts (all row-major, contiguous, device memory unless stated):
+ * Layouts (all row-major, contiguous, device memory unless stated; "fp16"
+ * reads bf16 when params.dtype is DECODE_ATTN_DTYPE_BF16):
  *   q           [B][Hq][D]              fp16   ([B][T][Hq][D] with num_queries T > 1)
  *   k_pages     [P][PS][Hkv][D]         fp16   (the caller's paged cache)
  *   v_pages     [P][PS][Hkv][D]         fp16
@@ -67,6 +68,10 @@ extern "C" {
 #define DECODE_ATTN_DEV_WORKSPACE 16    /* a group's shard ticket was not zero on entry:
                                            the group's rows may be stale; clear and retry */
 
+/* Element formats of q, k_pages, v_pages, out, k_new, v_new (params.dtype). */
+#define DECODE_ATTN_DTYPE_FP16 0        /* IEEE binary16 */
+#define DECODE_ATTN_DTYPE_BF16 1        /* bfloat16 (tensor-core variant) */
+
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
 #define DECODE_ATTN_VARIANT_SIMT 1      /* CUDA-core q.k / p.v with warp-shuffle reductions */
@@ -92,6 +97,8 @@ typedef struct decode_attn_params {
                                 sits at position seq_lens[b] - T + t and attends causally
                                 (up to itself; the window counted from it); needs
                                 T * G <= 16 and the tensor-core variant */
+  int32_t dtype;             /* DECODE_ATTN_DTYPE_*: element format of every 16-bit
+                                tensor; accumulation is fp32 for both */
 } decode_attn_params;
 
 /* Launch plan chosen by the host heuristic (exposed for inspection/tests). */

@@ -26,10 +26,11 @@ __all__ = [
     "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
-    "decode_kv_append", "decode_attn_append",
+    "decode_kv_append", "decode_attn_append", "DTYPE_FP16", "DTYPE_BF16",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
+DTYPE_FP16, DTYPE_BF16 = 0, 1
 DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -45,7 +46,7 @@ class DecodeAttnParams(ctypes.Structure):
         "max_pages_per_seq", "num_pages", "max_seq_len")] + [
         ("scale", ctypes.c_float), ("window", ctypes.c_int32), ("variant", ctypes.c_int32),
         ("split_min", ctypes.c_int32), ("force_chunk", ctypes.c_int32),
-        ("num_queries", ctypes.c_int32)]
+        ("num_queries", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 class DecodeAttnPlan(ctypes.Structure):
@@ -127,7 +128,19 @@ def make_params(q, k_pages, page_table, scale: float, window: int = 0,
         max_pages_per_seq=page_table.shape[1], num_pages=P,
         max_seq_len=int(max_seq_len) if max_seq_len else 0, scale=float(scale),
         window=int(window), variant=int(variant), split_min=int(split_min),
-        force_chunk=int(force_chunk), num_queries=int(T))
+        force_chunk=int(force_chunk), num_queries=int(T), dtype=_dtype_code(q))
+
+
+def _dtype_code(t) -> int:
+    """DTYPE_BF16 for torch.bfloat16 tensors, else DTYPE_FP16."""
+    return DTYPE_BF16 if str(getattr(t, "dtype", "")) == "torch.bfloat16" else DTYPE_FP16
+
+
+def _elem_dtype(t):
+    import torch
+    if t.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"expected float16 or bfloat16 tensors, got {t.dtype}")
+    return t.dtype
 
 
 def decode_attn_make_plan(params: DecodeAttnParams, num_sms: int) -> DecodeAttnPlan:
@@ -201,9 +214,10 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
     if dev.type != "cuda":
         raise ValueError("decode_attn runs on CUDA tensors (use decode_attn_host for host "
                          "buffers)")
-    _check(q, torch.float16, "q", dev)
-    _check(k_pages, torch.float16, "k_pages", dev)
-    _check(v_pages, torch.float16, "v_pages", dev)
+    et = _elem_dtype(q)
+    _check(q, et, "q", dev)
+    _check(k_pages, et, "k_pages", dev)
+    _check(v_pages, et, "v_pages", dev)
     _check(page_table, torch.int32, "page_table", dev)
     _check(seq_lens, torch.int32, "seq_lens", dev)
     if v_pages.shape != k_pages.shape:
@@ -212,7 +226,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
                     force_chunk)
     if out is None:
         out = torch.empty_like(q)
-    _check(out, torch.float16, "out", dev)
+    _check(out, et, "out", dev)
     need = decode_attn_workspace_size(p, dev.index if dev.index is not None else
                                       torch.cuda.current_device())
     if workspace is None:
@@ -249,11 +263,12 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
     (int32, -1 = none) into the paged pools, bit for bit."""
     import torch
     dev = k_pages.device
-    _check(k_new, torch.float16, "k_new", dev)
-    _check(v_new, torch.float16, "v_new", dev)
+    et = _elem_dtype(k_pages)
+    _check(k_new, et, "k_new", dev)
+    _check(v_new, et, "v_new", dev)
     _check(positions, torch.int32, "positions", dev)
-    _check(k_pages, torch.float16, "k_pages", dev)
-    _check(v_pages, torch.float16, "v_pages", dev)
+    _check(k_pages, et, "k_pages", dev)
+    _check(v_pages, et, "v_pages", dev)
     _check(page_table, torch.int32, "page_table", dev)
     P, PS, Hkv, D = k_pages.shape
     if tuple(k_new.shape) != (page_table.shape[0], Hkv, D) or v_new.shape != k_new.shape:
@@ -261,7 +276,7 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
     p = DecodeAttnParams(batch=page_table.shape[0], num_q_heads=Hkv, num_kv_heads=Hkv,
                          head_dim=D, page_size=PS, max_pages_per_seq=page_table.shape[1],
                          num_pages=P, max_seq_len=0, scale=1.0, window=0, variant=0,
-                         split_min=0, force_chunk=0, num_queries=1)
+                         split_min=0, force_chunk=0, num_queries=1, dtype=_dtype_code(k_pages))
     st = load_library().decode_kv_append(ctypes.byref(p), _ptr(k_new), _ptr(v_new),
                                          _ptr(positions), _ptr(k_pages), _ptr(v_pages),
                                          _ptr(page_table), _ptr(err_flag),
@@ -281,8 +296,8 @@ def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, 
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
                                     workspace)
-    _check(k_new, torch.float16, "k_new", q.device)
-    _check(v_new, torch.float16, "v_new", q.device)
+    _check(k_new, q.dtype, "k_new", q.device)
+    _check(v_new, q.dtype, "v_new", q.device)
     st = load_library().decode_attn_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
                                            _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
                                            _ptr(seq_lens), _ptr(out), _ptr(ws), ws_bytes,
@@ -359,13 +374,13 @@ def decode_attn_static_scratch(q, k_pages, v_pages, page_table, seq_lens, scale:
     Only ``out`` is created here when not given; pass it to allocate nothing."""
     import torch
     dev = q.device
-    for t, dt, n in ((q, torch.float16, "q"), (k_pages, torch.float16, "k_pages"),
-                     (v_pages, torch.float16, "v_pages"), (page_table, torch.int32, "page_table"),
-                     (seq_lens, torch.int32, "seq_lens")):
+    et = _elem_dtype(q)
+    for t, dt, n in ((q, et, "q"), (k_pages, et, "k_pages"), (v_pages, et, "v_pages"),
+                     (page_table, torch.int32, "page_table"), (seq_lens, torch.int32, "seq_lens")):
         _check(t, dt, n, dev)
     if out is None:
         out = torch.empty_like(q)
-    _check(out, torch.float16, "out", dev)
+    _check(out, et, "out", dev)
     p = make_params(q, k_pages, page_table, scale, window, max_seq_len, variant, split_min,
                     force_chunk)
     st = _static_scratch_fn()(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),

@@ -60,6 +60,8 @@ int check_params(const decode_attn_params* p) {
     return DECODE_ATTN_ERR_SHAPE;
   if (p->num_q_heads / p->num_kv_heads > 16) return DECODE_ATTN_ERR_GROUP;
   if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
+  if (p->dtype != DECODE_ATTN_DTYPE_FP16 && p->dtype != DECODE_ATTN_DTYPE_BF16)
+    return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -114,7 +116,7 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   if (variant == DECODE_ATTN_VARIANT_AUTO) variant = DECODE_ATTN_VARIANT_MMA;
   int group_pad = gp;
   if (variant == DECODE_ATTN_VARIANT_SIMT) {
-    if (gp > 8 || T > 1) return DECODE_ATTN_ERR_VARIANT;
+    if (gp > 8 || T > 1 || p->dtype != DECODE_ATTN_DTYPE_FP16) return DECODE_ATTN_ERR_VARIANT;
   } else if (variant == DECODE_ATTN_VARIANT_MMA) {
     const int rows = T * G;  // query rows per KV head: one or two n8 tiles
     if (rows > 16) return DECODE_ATTN_ERR_VARIANT;
@@ -215,7 +217,10 @@ int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p->num_kv_heads * D * 2};
   cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_t};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides,
+  const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
+                                    ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, et, 3, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
@@ -234,7 +239,10 @@ int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_at
   cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)p->num_kv_heads * D * 2};
   cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_t};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides,
+  const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
+                                    ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, et, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
@@ -296,18 +304,18 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   if (!st) st = encode(&L.tmap_v, v_pages, p, box_t);
   if (st) return st;
   SplitArgs& a = L.args;
-  a.q = static_cast<const __half*>(q);
+  a.q = q;
   a.page_table = page_table;
   a.seq_lens = seq_lens;
-  a.out = static_cast<__half*>(out);
+  a.out = out;
   a.ws_acc = ws.acc;
   a.ws_ml = ws.ml;
   a.counters = ws.counters;
   a.err = err_flag;
-  a.k_new = static_cast<const __half*>(k_new);
-  a.v_new = static_cast<const __half*>(v_new);
-  a.k_pages_w = static_cast<__half*>(const_cast<void*>(k_pages));
-  a.v_pages_w = static_cast<__half*>(const_cast<void*>(v_pages));
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_pages_w = const_cast<void*>(k_pages);
+  a.v_pages_w = const_cast<void*>(v_pages);
   a.Hq = p->num_q_heads;
   a.Hkv = p->num_kv_heads;
   a.G = p->num_q_heads / p->num_kv_heads;
@@ -325,6 +333,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.grid = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
   L.group_pad = plan.group_pad;
   L.variant = plan.variant;
+  L.dtype = p->dtype;
   L.stream = stream;
   // the shard tickets are zero on entry: the last CTA of each group clears
   // its own, so a workspace cleared once stays clear across calls
@@ -342,7 +351,7 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
   a.seq_lens = seq_lens;
   a.ws_acc = ws.acc;
   a.ws_ml = ws.ml;
-  a.out = static_cast<__half*>(out);
+  a.out = out;
   a.B = p->batch;
   a.Hq = p->num_q_heads;
   a.G = p->num_q_heads / p->num_kv_heads;
@@ -352,9 +361,9 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
   a.chunk = plan.chunk_tokens;
   a.max_shards = plan.max_shards;
   switch (p->head_dim) {
-    case 64: return cuda_status(launch_combine_d64(a, stream));
-    case 128: return cuda_status(launch_combine_d128(a, stream));
-    default: return cuda_status(launch_combine_d256(a, stream));
+    case 64: return cuda_status(launch_combine_d64(a, p->dtype, stream));
+    case 128: return cuda_status(launch_combine_d128(a, p->dtype, stream));
+    default: return cuda_status(launch_combine_d256(a, p->dtype, stream));
   }
 }
 

@@ -15,6 +15,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "elem.cuh"
 
 namespace pgd {
 
@@ -22,7 +23,7 @@ struct CombineArgs {
   const int32_t* seq_lens;
   const float* ws_acc;   // [B*T*Hq*S_max][D]
   const float2* ws_ml;   // [B*T*Hq*S_max]
-  __half* out;           // [B][T][Hq][D]
+  void* out;             // [B][T][Hq][D] 16-bit elements
   int32_t B, Hq, G, T, capacity, window, chunk, max_shards;
 };
 
@@ -52,7 +53,7 @@ __host__ __device__ constexpr int merge_smem_bytes(int G) {
 // (tid = this thread's index among them) and `smem` (merge_smem_bytes(G)
 // bytes, 16-byte aligned).  `sync` is a barrier over exactly those threads.
 // dead forces zero rows (an invalid range).
-template <int D, class Sync>
+template <int D, class E, class Sync>
 __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, int S, bool dead,
                                             int tid, int nthreads, uint8_t* smem, Sync sync) {
   constexpr int kQuads = D / 4;
@@ -160,11 +161,12 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     for (int k = 0; k < n_items; ++k) {
       const bool z = zero[k] || L[k] == 0.f;
       const float l_sum = L[k];
-      const __half2 lo = __floats2half2_rn(z ? 0.f : __fdiv_rn(o[k].x, l_sum),
-                                           z ? 0.f : __fdiv_rn(o[k].y, l_sum));
-      const __half2 hi = __floats2half2_rn(z ? 0.f : __fdiv_rn(o[k].z, l_sum),
-                                           z ? 0.f : __fdiv_rn(o[k].w, l_sum));
-      __half2* dst = reinterpret_cast<__half2*>(a.out + row[k] * D + 4 * quad[k]);
+      const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o[k].x, l_sum),
+                                            z ? 0.f : __fdiv_rn(o[k].y, l_sum));
+      const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o[k].z, l_sum),
+                                            z ? 0.f : __fdiv_rn(o[k].w, l_sum));
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row[k] * D + 4 * quad[k]);
       dst[0] = lo;
       dst[1] = hi;
     }
@@ -174,15 +176,15 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
 // Standalone combine: one CTA per (KV head, sequence).  Launched as a
 // programmatic dependent of the split kernel: waits (griddepcontrol.wait) for
 // the split grid's partials before reading them.
-template <int D>
+template <int D, class E>
 __global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(16) uint8_t merge_smem[];
   const int h = blockIdx.x, b = blockIdx.y;
   const SeqRange r =
       seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T);
   grid_dependency_wait();
-  merge_group<D>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
-                 [] { __syncthreads(); });
+  merge_group<D, E>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
+                    [] { __syncthreads(); });
 }
 
 }  // namespace pgd

@@ -18,15 +18,16 @@ struct SplitLaunch {
   dim3 grid;
   int group_pad;
   int variant;
+  int dtype;
   cudaStream_t stream;
 };
 
 cudaError_t launch_split_d64(const SplitLaunch& L);
 cudaError_t launch_split_d128(const SplitLaunch& L);
 cudaError_t launch_split_d256(const SplitLaunch& L);
-cudaError_t launch_combine_d64(const CombineArgs& a, cudaStream_t stream);
-cudaError_t launch_combine_d128(const CombineArgs& a, cudaStream_t stream);
-cudaError_t launch_combine_d256(const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_combine_d64(const CombineArgs& a, int dtype, cudaStream_t stream);
+cudaError_t launch_combine_d128(const CombineArgs& a, int dtype, cudaStream_t stream);
+cudaError_t launch_combine_d256(const CombineArgs& a, int dtype, cudaStream_t stream);
 
 struct KvAppendArgs {
   const uint4* k_new;   // [B][Hkv][D] as 16-byte chunks

@@ -9,7 +9,8 @@
 //   out^T    [D x 8 heads]     += V^T [D x 16 tok] . P^T [16 tok x 8 heads]
 // The score accumulator's fragment is transposed into the P^T operand with
 // movmatrix; P is split into an fp16 head and an fp16 remainder (two mma per
-// tile) so the weights keep about 22 bits, as the fp32 CUDA-core path does.
+// tile) so the weights keep about twice the element format's bits (22 for
+// fp16, 16 for bf16).  Templated on the element format E (fp16 or bf16).
 //
 // Shared-memory tiles are [D/64][64 tokens][64 dims] with the 128-byte TMA
 // swizzle (16-byte chunk c of token row t lives at chunk c ^ (t % 8)), so
@@ -44,24 +45,10 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                : "r"(addr));
 }
 
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                              uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -73,7 +60,7 @@ __device__ __forceinline__ uint32_t swz_offset(int t, int d) {
   return (uint32_t)((d >> 6) * (kTile * 128) + t * 128 + ((((d >> 3) & 7) ^ (t & 7)) << 4));
 }
 
-template <int D, int NT8>
+template <int D, int NT8, class E>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
@@ -196,7 +183,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
 #pragma unroll
   for (int j = 0; j < NT8; ++j) {
     const int rr = 8 * j + gid;
-    const __half* qrow = a.q + group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq) * D;
+    const uint16_t* qrow =
+        static_cast<const uint16_t*>(a.q) + group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       if (rr < R) {
@@ -276,7 +264,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
         uint32_t af[4];
         ldmatrix_x4(af, kbase + swz_offset(k_tok, ks * 16 + k_dof));
 #pragma unroll
-        for (int j = 0; j < NT8; ++j) mma_f16_16816(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
+        for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
       }
       // online softmax over this block's 16 positions
       const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
@@ -307,12 +295,12 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
           m_run[j][e] = m_new;
         }
         // P^T operand: fp16 head and fp16 remainder, transposed by movmatrix
-        const uint32_t h0 = pack_f16x2(p[0], p[1]);
-        const uint32_t h1 = pack_f16x2(p[2], p[3]);
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-        const uint32_t l0 = pack_f16x2(p[0] - f0.x, p[1] - f0.y);
-        const uint32_t l1 = pack_f16x2(p[2] - f1.x, p[3] - f1.y);
+        const uint32_t h0 = ElemOps<E>::pack2(p[0], p[1]);
+        const uint32_t h1 = ElemOps<E>::pack2(p[2], p[3]);
+        const float2 f0 = ElemOps<E>::unpack2(h0);
+        const float2 f1 = ElemOps<E>::unpack2(h1);
+        const uint32_t l0 = ElemOps<E>::pack2(p[0] - f0.x, p[1] - f0.y);
+        const uint32_t l1 = ElemOps<E>::pack2(p[2] - f1.x, p[3] - f1.y);
         pb_hi[j][0] = movmatrix_trans(h0);
         pb_hi[j][1] = movmatrix_trans(h1);
         pb_lo[j][0] = movmatrix_trans(l0);
@@ -336,8 +324,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
         ldmatrix_x4_trans(af, vbase + swz_offset(v_tok, mi * 16 + v_dof));
 #pragma unroll
         for (int j = 0; j < NT8; ++j) {
-          mma_f16_16816(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
-          mma_f16_16816(acc[mi][j], af, pb_lo[j][0], pb_lo[j][1]);
+          ElemOps<E>::mma(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
+          ElemOps<E>::mma(acc[mi][j], af, pb_lo[j][0], pb_lo[j][1]);
         }
       }
     }
@@ -395,14 +383,15 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     }
     const size_t row = group_row(b, h, g, a.T, G, a.Hq);
     if (!a.split) {
-      a.out[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
+      static_cast<uint16_t*>(a.out)[row * D + d] =
+          ElemOps<E>::round((dead || L == 0.f) ? 0.f : O / L);
     } else {
       const size_t slot = row * a.max_shards + s;
       a.ws_acc[slot * D + d] = dead ? 0.f : O;
       if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
     }
   }
-  if (a.split) merge_if_last<D>(a, r, b, h, ring, kWarps * 32);
+  if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
 }
 
 }  // namespace pgd

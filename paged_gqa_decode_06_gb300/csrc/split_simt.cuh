@@ -30,18 +30,18 @@
 namespace pgd {
 
 struct SplitArgs {
-  const __half* q;            // [B][Hq][D]
+  const void* q;              // [B][T][Hq][D] 16-bit elements (fp16 or bf16)
   const int32_t* page_table;  // [B][max_pages]
   const int32_t* seq_lens;    // [B]
-  __half* out;                // [B][Hq][D]          (single pass)
+  void* out;                  // [B][T][Hq][D]       (single pass and merge)
   float* ws_acc;              // [B*Hq*S_max][D]     (split)
   float2* ws_ml;              // [B*Hq*S_max] (m, l) (split; l = -1 marks a bad row)
   int32_t* counters;          // [B*Hkv] shards finished per group (split; zero on entry)
   int32_t* err;               // nullable
-  const __half* k_new;        // [B][Hkv][D] rows to append at seq_len - 1, or null
-  const __half* v_new;
-  __half* k_pages_w;          // the pool, written only when appending
-  __half* v_pages_w;
+  const void* k_new;          // [B][T][Hkv][D] rows to append at the last T positions, or null
+  const void* v_new;
+  void* k_pages_w;            // the pool, written only when appending
+  void* v_pages_w;
   int32_t Hq, Hkv, G;
   int32_t max_pages, num_pages, page_size, page_shift, box_tokens;
   int32_t window, chunk, max_shards, split;
@@ -102,9 +102,10 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 
 template <int D, int GP>
 __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h) {
+  uint16_t* out = static_cast<uint16_t*>(a.out);  // +0.0 is all zero bits in both formats
   for (int e = threadIdx.x; e < a.T * a.G * D; e += blockDim.x) {
     const int g = e / D, d = e % D;
-    a.out[group_row(b, h, g, a.T, a.G, a.Hq) * D + d] = __float2half_rn(0.f);
+    out[group_row(b, h, g, a.T, a.G, a.Hq) * D + d] = 0;
   }
 }
 
@@ -122,11 +123,13 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
     const size_t off =
         (((size_t)phys * a.page_size + (pos & (a.page_size - 1))) * a.Hkv + h) * D;
     const size_t src = (((size_t)b * a.T + i) * a.Hkv + h) * D;
+    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.k_new) + src);
+    const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v_new) + src);
+    uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.k_pages_w) + off);
+    uint4* vd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.v_pages_w) + off);
     for (int c = lane; c < D / 8; c += 32) {
-      reinterpret_cast<uint4*>(a.k_pages_w + off)[c] =
-          reinterpret_cast<const uint4*>(a.k_new + src)[c];
-      reinterpret_cast<uint4*>(a.v_pages_w + off)[c] =
-          reinterpret_cast<const uint4*>(a.v_new + src)[c];
+      kd[c] = ks[c];
+      vd[c] = vs[c];
     }
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -137,7 +140,7 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
 // CTA's partial is written: the last CTA of the group to finish (an atomic
 // ticket; no CTA ever waits on another) merges the group's partials into the
 // output in ascending shard order and clears the ticket for the next call.
-template <int D>
+template <int D, class E = __half>
 __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange& r, int b, int h,
                                               uint8_t* smem, int nthreads) {
   __shared__ int is_last_s;
@@ -165,8 +168,8 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   c.window = a.window;
   c.chunk = a.chunk;
   c.max_shards = a.max_shards;
-  merge_group<D>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem,
-                 [nthreads] { named_barrier_sync(1, nthreads); });
+  merge_group<D, E>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem,
+                    [nthreads] { named_barrier_sync(1, nthreads); });
   if (threadIdx.x == 0) *ticket = 0;
 }
 
@@ -293,7 +296,9 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     if (g < G) {
-      load_f16_row<DPL>(a.q + ((size_t)b * a.Hq + h * G + g) * D + lane * DPL, qf[g]);
+      load_f16_row<DPL>(static_cast<const __half*>(a.q) + ((size_t)b * a.Hq + h * G + g) * D +
+                            lane * DPL,
+                        qf[g]);
     } else {
 #pragma unroll
       for (int i = 0; i < DPL; ++i) qf[g][i] = 0.f;
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
     }
     const size_t row = (size_t)b * a.Hq + h * G + g;
     if (!a.split) {
-      a.out[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
+      static_cast<__half*>(a.out)[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
     } else {
       const size_t slot = row * a.max_shards + s;
       a.ws_acc[slot * D + d] = dead ? 0.f : O;

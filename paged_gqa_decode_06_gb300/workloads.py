@@ -82,22 +82,24 @@ class Workload:
             seq_lens=self.seq_lens.to(device))
 
 
-def _randn_fp16(shape, gen: torch.Generator, device) -> torch.Tensor:
-    """N(0,1) drawn in fp32, rounded to fp16; drawn in slabs to bound the fp32
-    temporary for the multi-GiB pools."""
-    out = torch.empty(shape, dtype=torch.float16, device=device)
+def _randn_fp16(shape, gen: torch.Generator, device, dtype=torch.float16) -> torch.Tensor:
+    """N(0,1) drawn in fp32, rounded to the 16-bit format (fp16 by default);
+    drawn in slabs to bound the fp32 temporary for the multi-GiB pools."""
+    out = torch.empty(shape, dtype=dtype, device=device)
     flat = out.view(-1)
     slab = 1 << 26
     for i in range(0, flat.numel(), slab):
         n = min(slab, flat.numel() - i)
-        flat[i:i + n] = torch.randn(n, generator=gen, device=device, dtype=torch.float32).half()
+        flat[i:i + n] = torch.randn(n, generator=gen, device=device,
+                                    dtype=torch.float32).to(dtype)
     return out
 
 
 def make_custom(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                 page_size: int, seq_lens: Sequence[int] | torch.Tensor, seed: int,
                 decoy_pages: int = 0, max_pages: Optional[int] = None, window: int = 0,
-                scale: Optional[float] = None, device="cpu") -> Workload:
+                scale: Optional[float] = None, device="cpu",
+                dtype=torch.float16) -> Workload:
     """General generator: pages of all sequences drawn without reuse from one
     pool of sum(ceil(L_b/PS)) + decoy_pages pages, by a seeded permutation."""
     device = torch.device(device)
@@ -109,9 +111,9 @@ def make_custom(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int, h
     mp = max_pages if max_pages is not None else max(need + [1])
     assert mp >= max(need + [0])
     P = sum(need) + decoy_pages
-    q = _randn_fp16((batch, num_q_heads, head_dim), gen, device)
-    k = _randn_fp16((P, page_size, num_kv_heads, head_dim), gen, device)
-    v = _randn_fp16((P, page_size, num_kv_heads, head_dim), gen, device)
+    q = _randn_fp16((batch, num_q_heads, head_dim), gen, device, dtype)
+    k = _randn_fp16((P, page_size, num_kv_heads, head_dim), gen, device, dtype)
+    v = _randn_fp16((P, page_size, num_kv_heads, head_dim), gen, device, dtype)
     perm = torch.randperm(P, generator=gen, device=device).to("cpu").to(torch.int32)
     table = torch.full((batch, mp), -1, dtype=torch.int32)
     off = 0
@@ -164,17 +166,18 @@ def batched_seq_lens(seed: int = 3, batch: int = 64, max_len: int = 8192) -> tor
     return torch.randint(1, max_len + 1, (batch,), generator=g, dtype=torch.int64)
 
 
-def make(name: str, device="cpu") -> Workload:
-    """One of the named workloads, drawn on ``device``."""
+def make(name: str, device="cpu", dtype=torch.float16) -> Workload:
+    """One of the named workloads, drawn on ``device`` (16-bit format
+    ``dtype``: torch.float16 or torch.bfloat16)."""
     if name == "batched":
         L = batched_seq_lens()
         need = int(sum((int(x) + 15) // 16 for x in L))
         return make_custom("batched", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
                            page_size=16, seq_lens=L, seed=3, decoy_pages=need // 10,
-                           max_pages=512, device=device)
+                           max_pages=512, device=device, dtype=dtype)
     if name.startswith("ctx"):  # e.g. "ctx300_d128": short-context sweep point
         ctx, shape = name[3:].split("_")
         return make_custom(name, batch=1, page_size=16, seq_lens=[int(ctx)], seed=5,
-                           decoy_pages=8, device=device, **SWEEP_SHAPES[shape])
+                           decoy_pages=8, device=device, dtype=dtype, **SWEEP_SHAPES[shape])
     kw = dict(CONFIGS[name])
-    return make_custom(name, device=device, **kw)
+    return make_custom(name, device=device, dtype=dtype, **kw)

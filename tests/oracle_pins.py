@@ -341,7 +341,8 @@ def check_multi_query(o):
 def bf16_bits_to_f64(bits):
     """bfloat16 is the upper half of an IEEE binary32: decode through numpy's
     float32."""
-    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN codes stay NaN
+        return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def check_bf16(o):

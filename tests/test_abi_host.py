@@ -55,7 +55,7 @@ def test_library_needs_no_driver_at_load(pkg):
 def params(pkg, **kw):
     base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                 max_pages_per_seq=192, num_pages=256, max_seq_len=3060, scale=0.088,
-                window=0, variant=0, split_min=0, force_chunk=0, num_queries=1)
+                window=0, variant=0, split_min=0, force_chunk=0, num_queries=1, dtype=0)
     base.update(kw)
     return pkg.DecodeAttnParams(**base)
 
@@ -233,3 +233,11 @@ def test_multi_query_plans(pkg):
     one = pkg.decode_attn_make_plan(params(pkg, num_queries=1), 152)
     four = pkg.decode_attn_make_plan(params(pkg, num_queries=4), 152)
     assert four.workspace_bytes - 65536 >= 4 * (one.workspace_bytes - 65536) - 4096
+
+
+def test_bf16_plans(pkg):
+    plan = pkg.decode_attn_make_plan(params(pkg, dtype=1), 152)
+    assert plan.variant == 2
+    for bad in (dict(dtype=1, variant=1), dict(dtype=2)):
+        with pytest.raises(pkg.DecodeAttnError):
+            pkg.decode_attn_make_plan(params(pkg, **bad), 152)
