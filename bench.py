@@ -62,6 +62,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", type=int, default=0)
     ap.add_argument("--force-chunk", type=int, default=0)
+    ap.add_argument("--dtype", default="fp16", choices=["fp16", "bf16"],
+                    help="element format of q, K/V and out")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query positions per sequence (the last T positions, causal)")
+    ap.add_argument("--append", action="store_true",
+                    help="time the fused append + attention launch (new rows at the last "
+                         "T positions)")
     ap.add_argument("--eager", action="store_true",
                     help="launch each step from the host instead of replaying a CUDA graph")
     return ap.parse_args(argv)
@@ -289,9 +296,26 @@ def gpu_arm(args):
     build.build()
     pkg.load_library()
 
-    w = workloads.make(args.workload, device=dev)
+    edt = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    w = workloads.make(args.workload, device=dev, dtype=edt)
+    T = max(1, args.queries)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    if T > 1:  # T query positions per sequence: q [B, T, Hq, D]
+        w.q = torch.randn(w.batch, T, w.num_q_heads, w.head_dim, generator=gen, device=dev,
+                          dtype=torch.float32).to(edt)
+    k_new = v_new = None
+    if args.append:
+        shape = (w.batch, T, w.num_kv_heads, w.head_dim) if T > 1 else \
+            (w.batch, w.num_kv_heads, w.head_dim)
+        k_new = torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(edt)
+        v_new = torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(edt)
     max_len = w.max_seq_len()
     kv_bytes = w.kv_bytes()
+    if T > 1 and w.window > 0:  # the first query's window starts T - 1 earlier
+        L = w.seq_lens.to("cpu").to(torch.int64)
+        kv_bytes = int(torch.clamp(L, max=w.window + T - 1).sum()) * w.num_kv_heads * \
+            w.head_dim * 4
     params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, w.window, max_len,
                              args.variant, 0, args.force_chunk)
     props = torch.cuda.get_device_properties(dev)
@@ -314,6 +338,12 @@ def gpu_arm(args):
         flush_read.sum()
 
     def split_call():
+        if args.append:
+            pkg.decode_attn_append(w.q, k_new, v_new, w.k_pages, w.v_pages, w.page_table,
+                                   w.seq_lens, w.scale, window=w.window, out=out,
+                                   max_seq_len=max_len, workspace=ws, err_flag=err,
+                                   variant=args.variant, force_chunk=args.force_chunk)
+            return
         pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
                               window=w.window, out=out, max_seq_len=max_len, workspace=ws,
                               err_flag=err, variant=args.variant, force_chunk=args.force_chunk)
@@ -401,7 +431,7 @@ def gpu_arm(args):
     traffic = recorded_traffic(args.workload)
     # ---- end to end from pinned host buffers through the C ABI
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and T == 1 and not args.append:
         pin = lambda t: t.to("cpu").contiguous().pin_memory()
         qh, kh, vh, th, lh = map(pin, (w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens))
         out_h = torch.empty_like(qh).pin_memory()
@@ -446,8 +476,10 @@ def gpu_arm(args):
             "steps": K, "warmup": args.warmup, "ms_per_step": ms_max,
             "us_per_step": ms_max * 1e3, "hbm_frac": value_tbs * 1e3 / peak_gbs,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp16 in / fp32 accumulate", "data": "synthetic (seeded N(0,1) fp16)",
+            "dtype": f"{args.dtype} in / fp32 accumulate",
+            "data": f"synthetic (seeded N(0,1) {args.dtype})",
             "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload],
+                       "queries_per_seq": T, "fused_append": bool(args.append),
                        "kv_bytes_per_step": kv_bytes, "resident_kv_bytes": resident,
                        "l2": ("flushed between timed steps (write of 4x L2, then read of 4x L2)" if flush else
                               f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"),

@@ -31,7 +31,7 @@ import torch
 @dataclasses.dataclass
 class Workload:
     name: str
-    q: torch.Tensor            # [B, Hq, D] fp16
+    q: torch.Tensor            # [B, Hq, D] (or [B, T, Hq, D]) fp16 / bf16
     k_pages: torch.Tensor      # [P, PS, Hkv, D] fp16
     v_pages: torch.Tensor      # [P, PS, Hkv, D] fp16
     page_table: torch.Tensor   # [B, max_pages] int32
@@ -46,11 +46,11 @@ class Workload:
 
     @property
     def num_q_heads(self) -> int:
-        return self.q.shape[1]
+        return self.q.shape[-2]  # q is [B, Hq, D] or [B, T, Hq, D]
 
     @property
     def head_dim(self) -> int:
-        return self.q.shape[2]
+        return self.q.shape[-1]
 
     @property
     def num_kv_heads(self) -> int:
