@@ -46,6 +46,7 @@ WORKLOAD_DESC = {
     "sweep_d128": "B=1, Hq=32, Hkv=8, D=128, context 3060, page 16",
     "sweep_d256": "B=1, Hq=16, Hkv=4, D=256, context 3060, page 16",
     "tiny": "B=1, Hq=4, Hkv=1, D=64, context 256, page 16",
+    "many_short": "B=1000, Hq=32, Hkv=8, D=128, seq_lens U[1,512], page 16",
 }
 
 
@@ -69,6 +70,8 @@ def parse_args(argv=None):
     ap.add_argument("--append", action="store_true",
                     help="time the fused append + attention launch (new rows at the last "
                          "T positions)")
+    ap.add_argument("--schedule", type=int, default=0,
+                    help="0 planner, 1 grid, 2 persistent balanced")
     ap.add_argument("--eager", action="store_true",
                     help="launch each step from the host instead of replaying a CUDA graph")
     return ap.parse_args(argv)
@@ -317,7 +320,7 @@ def gpu_arm(args):
         kv_bytes = int(torch.clamp(L, max=w.window + T - 1).sum()) * w.num_kv_heads * \
             w.head_dim * 4
     params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, w.window, max_len,
-                             args.variant, 0, args.force_chunk)
+                             args.variant, 0, args.force_chunk, args.schedule)
     props = torch.cuda.get_device_properties(dev)
     plan = pkg.decode_attn_make_plan(params, props.multi_processor_count)
     ws_bytes = pkg.decode_attn_workspace_size(params, local)
@@ -342,11 +345,13 @@ def gpu_arm(args):
             pkg.decode_attn_append(w.q, k_new, v_new, w.k_pages, w.v_pages, w.page_table,
                                    w.seq_lens, w.scale, window=w.window, out=out,
                                    max_seq_len=max_len, workspace=ws, err_flag=err,
-                                   variant=args.variant, force_chunk=args.force_chunk)
+                                   variant=args.variant, force_chunk=args.force_chunk,
+                                   schedule=args.schedule)
             return
         pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
                               window=w.window, out=out, max_seq_len=max_len, workspace=ws,
-                              err_flag=err, variant=args.variant, force_chunk=args.force_chunk)
+                              err_flag=err, variant=args.variant, force_chunk=args.force_chunk,
+                              schedule=args.schedule)
 
     def step_call():
         # one launch: the split kernel's last CTA per group merges the partials

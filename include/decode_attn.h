@@ -72,6 +72,13 @@ extern "C" {
 #define DECODE_ATTN_DTYPE_FP16 0        /* IEEE binary16 */
 #define DECODE_ATTN_DTYPE_BF16 1        /* bfloat16 (tensor-core variant) */
 
+/* Work schedules of the split kernel (decode_attn_params.schedule). */
+#define DECODE_ATTN_SCHEDULE_AUTO 0       /* planner picks (the grid schedule) */
+#define DECODE_ATTN_SCHEDULE_GRID 1       /* one CTA per (shard, KV head, sequence) */
+#define DECODE_ATTN_SCHEDULE_PERSISTENT 2 /* one CTA per resident slot, equal tile ranges
+                                             of the flattened (sequence, KV head, tile) list;
+                                             tensor-core variant, B <= 1024 */
+
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
 #define DECODE_ATTN_VARIANT_SIMT 1      /* CUDA-core q.k / p.v with warp-shuffle reductions */
@@ -99,6 +106,7 @@ typedef struct decode_attn_params {
                                 T * G <= 16 and the tensor-core variant */
   int32_t dtype;             /* DECODE_ATTN_DTYPE_*: element format of every 16-bit
                                 tensor; accumulation is fp32 for both */
+  int32_t schedule;          /* DECODE_ATTN_SCHEDULE_*; 0 = automatic */
 } decode_attn_params;
 
 /* Launch plan chosen by the host heuristic (exposed for inspection/tests). */
@@ -111,6 +119,8 @@ typedef struct decode_attn_plan {
   int32_t max_shards;        /* S_max: shards of the longest planned sequence */
   int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (shard, kv head, batch) */
   int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
+  int32_t persistent;        /* 1: persistent balanced schedule (grid_x = CTAs, slots
+                                of 2 partials per CTA); 0: grid schedule */
   size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;

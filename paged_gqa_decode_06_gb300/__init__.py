@@ -27,9 +27,11 @@ __all__ = [
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
     "decode_kv_append", "decode_attn_append", "DTYPE_FP16", "DTYPE_BF16",
+    "SCHEDULE_AUTO", "SCHEDULE_GRID", "SCHEDULE_PERSISTENT",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
+SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_PERSISTENT = 0, 1, 2
 DTYPE_FP16, DTYPE_BF16 = 0, 1
 DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
 
@@ -46,13 +48,15 @@ class DecodeAttnParams(ctypes.Structure):
         "max_pages_per_seq", "num_pages", "max_seq_len")] + [
         ("scale", ctypes.c_float), ("window", ctypes.c_int32), ("variant", ctypes.c_int32),
         ("split_min", ctypes.c_int32), ("force_chunk", ctypes.c_int32),
-        ("num_queries", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+        ("num_queries", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("schedule", ctypes.c_int32)]
 
 
 class DecodeAttnPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "split", "variant", "group_pad", "tile_tokens", "chunk_tokens", "max_shards",
-        "grid_x", "grid_y", "grid_z", "ctas_per_sm")] + [("workspace_bytes", ctypes.c_size_t)]
+        "grid_x", "grid_y", "grid_z", "ctas_per_sm", "persistent")] + [
+        ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -111,7 +115,8 @@ def decode_attn_strerror(code: int) -> str:
 
 def make_params(q, k_pages, page_table, scale: float, window: int = 0,
                 max_seq_len: Optional[int] = None, variant: int = VARIANT_AUTO,
-                split_min: int = 0, force_chunk: int = 0) -> DecodeAttnParams:
+                split_min: int = 0, force_chunk: int = 0,
+                schedule: int = SCHEDULE_AUTO) -> DecodeAttnParams:
     """Parameters from tensor shapes: q [B,Hq,D] (or [B,T,Hq,D] for T query
     positions per sequence), k_pages [P,PS,Hkv,D], page_table [B,maxPages].
     ``max_seq_len`` is a host-side bound on seq_lens (it sizes the grid;
@@ -128,7 +133,8 @@ def make_params(q, k_pages, page_table, scale: float, window: int = 0,
         max_pages_per_seq=page_table.shape[1], num_pages=P,
         max_seq_len=int(max_seq_len) if max_seq_len else 0, scale=float(scale),
         window=int(window), variant=int(variant), split_min=int(split_min),
-        force_chunk=int(force_chunk), num_queries=int(T), dtype=_dtype_code(q))
+        force_chunk=int(force_chunk), num_queries=int(T), dtype=_dtype_code(q),
+        schedule=int(schedule))
 
 
 def _dtype_code(t) -> int:
@@ -208,7 +214,7 @@ def _stream_handle(stream) -> int:
 
 
 def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_seq_len,
-             variant, split_min, force_chunk, workspace):
+             variant, split_min, force_chunk, workspace, schedule=SCHEDULE_AUTO):
     import torch
     dev = q.device
     if dev.type != "cuda":
@@ -223,7 +229,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
     if v_pages.shape != k_pages.shape:
         raise ValueError("k_pages and v_pages shapes differ")
     p = make_params(q, k_pages, page_table, scale, window, max_seq_len, variant, split_min,
-                    force_chunk)
+                    force_chunk, schedule)
     if out is None:
         out = torch.empty_like(q)
     _check(out, et, "out", dev)
@@ -238,7 +244,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
 def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
                 out=None, max_seq_len: Optional[int] = None, workspace=None, err_flag=None,
                 variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
-                stream=None):
+                stream=None, schedule: int = SCHEDULE_AUTO):
     """One decode step of paged GQA attention; returns ``out`` [B,Hq,D] fp16.
 
     q [B,Hq,D] fp16, k_pages/v_pages [P,PS,Hkv,D] fp16, page_table [B,maxPages]
@@ -248,7 +254,7 @@ def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window:
     (default: torch's current stream); does not synchronise."""
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace)
+                                    workspace, schedule)
     st = load_library().decode_attn(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                     _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(ws),
                                     ws_bytes, _ptr(err_flag), _stream_handle(stream))
@@ -276,7 +282,8 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
     p = DecodeAttnParams(batch=page_table.shape[0], num_q_heads=Hkv, num_kv_heads=Hkv,
                          head_dim=D, page_size=PS, max_pages_per_seq=page_table.shape[1],
                          num_pages=P, max_seq_len=0, scale=1.0, window=0, variant=0,
-                         split_min=0, force_chunk=0, num_queries=1, dtype=_dtype_code(k_pages))
+                         split_min=0, force_chunk=0, num_queries=1, dtype=_dtype_code(k_pages),
+                         schedule=0)
     st = load_library().decode_kv_append(ctypes.byref(p), _ptr(k_new), _ptr(v_new),
                                          _ptr(positions), _ptr(k_pages), _ptr(v_pages),
                                          _ptr(page_table), _ptr(err_flag),
@@ -288,14 +295,15 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
 def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, scale: float,
                        window: int = 0, out=None, max_seq_len: Optional[int] = None,
                        workspace=None, err_flag=None, variant: int = VARIANT_AUTO,
-                       split_min: int = 0, force_chunk: int = 0, stream=None):
+                       split_min: int = 0, force_chunk: int = 0, stream=None,
+                       schedule: int = SCHEDULE_AUTO):
     """Append + attention in one launch: writes k_new/v_new [B,Hkv,D] (or
     [B,T,Hkv,D] with q [B,T,Hq,D]) at the last T positions of each sequence
     (seq_lens counts them), then attends as decode_attn."""
     import torch
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace)
+                                    workspace, schedule)
     _check(k_new, q.dtype, "k_new", q.device)
     _check(v_new, q.dtype, "v_new", q.device)
     st = load_library().decode_attn_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
@@ -310,12 +318,12 @@ def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, 
 def decode_attn_split(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
                       out=None, max_seq_len=None, workspace=None, err_flag=None,
                       variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
-                      stream=None):
+                      stream=None, schedule: int = SCHEDULE_AUTO):
     """The shard kernel alone (writes ``out`` directly for a single-pass plan,
     partials into ``workspace`` otherwise).  Returns (out, workspace)."""
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace)
+                                    workspace, schedule)
     st = load_library().decode_attn_split(ctypes.byref(p), _ptr(q), _ptr(k_pages),
                                           _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
                                           _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
@@ -367,7 +375,8 @@ def _static_scratch_fn():
 def decode_attn_static_scratch(q, k_pages, v_pages, page_table, seq_lens, scale: float,
                                window: int = 0, out=None, max_seq_len: Optional[int] = None,
                                err_flag=None, variant: int = VARIANT_AUTO, split_min: int = 0,
-                               force_chunk: int = 0, stream=None):
+                               force_chunk: int = 0, stream=None,
+                               schedule: int = SCHEDULE_AUTO):
     """decode_attn for callers that cannot allocate device memory: the shard
     partials use the library's fixed 8 MiB device array instead of a
     workspace (shared by all calls on a device; overlapping calls race).
@@ -382,7 +391,7 @@ def decode_attn_static_scratch(q, k_pages, v_pages, page_table, seq_lens, scale:
         out = torch.empty_like(q)
     _check(out, et, "out", dev)
     p = make_params(q, k_pages, page_table, scale, window, max_seq_len, variant, split_min,
-                    force_chunk)
+                    force_chunk, schedule)
     st = _static_scratch_fn()(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                               _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(err_flag),
                               _stream_handle(stream))

@@ -62,6 +62,7 @@ int check_params(const decode_attn_params* p) {
   if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
   if (p->dtype != DECODE_ATTN_DTYPE_FP16 && p->dtype != DECODE_ATTN_DTYPE_BF16)
     return DECODE_ATTN_ERR_SHAPE;
+  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_PERSISTENT) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -91,6 +92,13 @@ size_t simt_smem_bytes(int head_dim) {
     case 64: return SimtCfg<64>::kSmemBytes;
     case 128: return SimtCfg<128>::kSmemBytes;
     default: return SimtCfg<256>::kSmemBytes;
+  }
+}
+int persist_smem(int head_dim, int nt8) {
+  switch (head_dim) {
+    case 64: return persist_smem_d64(nt8);
+    case 128: return persist_smem_d128(nt8);
+    default: return persist_smem_d256(nt8);
   }
 }
 int simt_ctas_per_sm(int head_dim) {
@@ -170,6 +178,48 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
   const int64_t max_shards = ceil_div(span, chunk);
   if (max_shards > 65535) return DECODE_ATTN_ERR_SHAPE;
+
+  // Persistent balanced schedule (one CTA per resident slot, equal tile
+  // ranges per KV head) only on request: on GB300 it measured level with the
+  // grid schedule on the batched mix (197.9 vs 197.7 us), behind it on the
+  // long context (317.9 vs 314.2 us) and well behind on a thousand short
+  // sequences (367 vs 217 us), where its per-segment fold and merge cost more
+  // than the grid's extra CTAs.
+  const int64_t units_all = (int64_t)p->batch * p->num_kv_heads;
+  const int64_t tiles_bound = units_all * ceil_div(span, kTile);
+  const bool persist_ok = variant == DECODE_ATTN_VARIANT_MMA && p->batch >= 1 &&
+                          p->batch <= kPersistMaxBatch && units_all <= 16384 &&
+                          tiles_bound < (int64_t(1) << 30) && p->num_kv_heads <= num_sms;
+  const bool large_work = units_all * span * 4 * p->head_dim > (int64_t)num_sms * ctas_per_sm *
+                                                                   (int64_t(1) << 20);
+  bool persistent = false;
+  if (p->schedule == DECODE_ATTN_SCHEDULE_PERSISTENT) {
+    if (!persist_ok) return DECODE_ATTN_ERR_VARIANT;
+    persistent = true;
+  }
+  (void)large_work;
+  if (persistent) {
+    // dynamic + static shared memory + the per-CTA reservation; the launch
+    // uses the device's own occupancy figure, never more CTAs than planned
+    const int per_cta = persist_smem(p->head_dim, group_pad / 8) + 7 * 1024 + 512;
+    const int cps = std::max(1, kSmemPerSm / per_cta);
+    const int64_t nc = (int64_t)num_sms * cps;
+    const size_t slots = (size_t)nc * 2 * T * G;
+    plan->variant = variant;
+    plan->group_pad = group_pad;
+    plan->tile_tokens = kTile;
+    plan->chunk_tokens = kTile;
+    plan->max_shards = 0;
+    plan->split = 1;
+    plan->persistent = 1;
+    plan->grid_x = (int32_t)nc;
+    plan->grid_y = 1;
+    plan->grid_z = 1;
+    plan->ctas_per_sm = cps;
+    plan->workspace_bytes = ticket_region_bytes(p) + round_up(slots * sizeof(float2), 256) +
+                            round_up(slots * p->head_dim * 4, 256);
+    return DECODE_ATTN_OK;
+  }
 
   plan->variant = variant;
   plan->group_pad = group_pad;
@@ -278,7 +328,11 @@ int workspace_views(const decode_attn_params* p, const decode_attn_plan& plan, v
   if (!plan.split) return DECODE_ATTN_OK;
   if (!ws || ws_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
     return DECODE_ATTN_ERR_WORKSPACE;
-  const size_t rows = (size_t)p->batch * num_queries(p) * p->num_q_heads * (size_t)plan.max_shards;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  const size_t rows = plan.persistent
+                          ? (size_t)plan.grid_x * 2 * num_queries(p) * G
+                          : (size_t)p->batch * num_queries(p) * p->num_q_heads *
+                                (size_t)plan.max_shards;
   char* base = static_cast<char*>(ws);
   const size_t tickets = ticket_region_bytes(p);
   const size_t ml_bytes = round_up(rows * sizeof(float2), 256);
@@ -334,6 +388,9 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.group_pad = plan.group_pad;
   L.variant = plan.variant;
   L.dtype = p->dtype;
+  L.persistent = plan.persistent;
+  L.batch = p->batch;
+  L.num_sms = plan.ctas_per_sm > 0 ? plan.grid_x / plan.ctas_per_sm : plan.grid_x;
   L.stream = stream;
   // the shard tickets are zero on entry: the last CTA of each group clears
   // its own, so a workspace cleared once stays clear across calls
@@ -347,6 +404,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
 int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
                 const int32_t* seq_lens, void* out, const Workspace& ws, cudaStream_t stream) {
   if (!plan.split || p->batch == 0) return DECODE_ATTN_OK;
+  if (plan.persistent) return DECODE_ATTN_OK;  // its merges ran inside the split launch
   CombineArgs a;
   a.seq_lens = seq_lens;
   a.ws_acc = ws.acc;

@@ -42,25 +42,40 @@ __device__ __forceinline__ void grid_launch_dependents() {
 }
 
 constexpr int kShardBlock = 256;   // (m, l) entries of each row staged per pass
-constexpr int kMaxMergeRows = 16;  // rows of one group (G <= 16)
+constexpr int kMaxMergeRows = 16;  // rows of one group (T * G <= 16)
 
-// Shared memory merge_group needs: staged (m, l) plus per-row max and flag.
-__host__ __device__ constexpr int merge_smem_bytes(int G) {
-  return G * kShardBlock * 8 + kMaxMergeRows * 8;
+// Shared memory merge_group needs when it stages `cap` (m, l) entries per
+// row: the staged pairs plus a per-row max and flag.
+__host__ __device__ constexpr int merge_smem_bytes(int rows, int cap = kShardBlock) {
+  return rows * cap * 8 + kMaxMergeRows * 8;
 }
 
-// Merges the S shards of group (b, h) (its T*G query rows) into out, using threads [0, nthreads)
-// (tid = this thread's index among them) and `smem` (merge_smem_bytes(G)
-// bytes, 16-byte aligned).  `sync` is a barrier over exactly those threads.
-// dead forces zero rows (an invalid range).
-template <int D, class E, class Sync>
+// Partial slots of the grid schedule: row-major over (row, shard).
+struct GridSlots {
+  int b, h, T, G, Hq, max_shards;
+  __device__ size_t operator()(int r, int s) const {
+    return group_row(b, h, r, T, G, Hq) * (size_t)max_shards + s;
+  }
+};
+
+// Merges the S shard partials of group (b, h) (its T*G query rows) into
+// out, in ascending shard order, using threads [0, nthreads) (tid = this
+// thread's index among them) and `smem` (merge_smem_bytes(rows, cap)
+// bytes, 16-byte aligned; up to `cap` (m, l) pairs per row are staged there,
+// more are read from global memory).  `sync` is a barrier over exactly those
+// threads; slot_of(r, s) locates the partial of row r, shard s.  dead forces
+// zero rows (an invalid range).
+template <int D, class E, class Sync, class SlotOf>
 __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, int S, bool dead,
-                                            int tid, int nthreads, uint8_t* smem, Sync sync) {
+                                            int tid, int nthreads, uint8_t* smem, int cap,
+                                            Sync sync, SlotOf slot_of) {
   constexpr int kQuads = D / 4;
   const int G = a.T * a.G;  // rows of the group
-  float2* ml_s = reinterpret_cast<float2*>(smem);                       // [G][kShardBlock]
-  float* max_s = reinterpret_cast<float*>(smem + G * kShardBlock * 8);  // [G]
-  int* zero_s = reinterpret_cast<int*>(max_s + kMaxMergeRows);          // [G]
+  float2* ml_s = reinterpret_cast<float2*>(smem);                // [G][cap]
+  float* max_s = reinterpret_cast<float*>(smem + G * cap * 8);   // [G]
+  int* zero_s = reinterpret_cast<int*>(max_s + kMaxMergeRows);   // [G]
+  const bool staged = S <= cap;
+  const int block = cap > 0 ? cap : 1;
 
   // per-row maximum and bad-partial flag, from (m, l) staged block by block
   sync();
@@ -68,20 +83,20 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     max_s[tid] = -INFINITY;
     zero_s[tid] = (dead || S == 0) ? 1 : 0;
   }
-  for (int s0 = 0; s0 < S; s0 += kShardBlock) {
-    const int n = min(kShardBlock, S - s0);
+  for (int s0 = 0; s0 < S; s0 += block) {
+    const int n = min(block, S - s0);
     sync();
-    for (int e = tid; e < G * n; e += nthreads) {
-      const int g = e / n, j = e % n;
-      ml_s[g * kShardBlock + j] =
-          __ldcg(a.ws_ml + group_row(b, h, g, a.T, a.G, a.Hq) * a.max_shards + s0 + j);
-    }
+    if (cap > 0)
+      for (int e = tid; e < G * n; e += nthreads) {
+        const int g = e / n, j = e % n;
+        ml_s[g * cap + j] = __ldcg(a.ws_ml + slot_of(g, s0 + j));
+      }
     sync();
     if (tid < G) {
       float M = max_s[tid];
       int z = zero_s[tid];
       for (int j = 0; j < n; ++j) {
-        const float2 v = ml_s[tid * kShardBlock + j];
+        const float2 v = cap > 0 ? ml_s[tid * cap + j] : __ldcg(a.ws_ml + slot_of(tid, s0 + j));
         z |= v.y < 0.f ? 1 : 0;  // a shard saw a bad page or gave up waiting
         M = fmaxf(M, v.x);
       }
@@ -93,7 +108,6 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
 
   // two output items (row, 4 dims) per thread and pass, their shard loads
   // issued together so several L2 round trips overlap
-  const bool staged = S <= kShardBlock;
   const int total = G * kQuads;
   for (int e0 = tid; e0 < total; e0 += 2 * nthreads) {
     int e[2] = {e0, e0 + nthreads};
@@ -102,22 +116,15 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     float4 o[2];
     float L[2], M[2];
     bool zero[2];
-    const float2* ml[2];
-    const float4* acc[2];
-    size_t row[2];
-    int quad[2];
+    int gg[2], quad[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int g = e[k] / kQuads;
+      gg[k] = e[k] / kQuads;
       quad[k] = e[k] % kQuads;
-      row[k] = group_row(b, h, g, a.T, a.G, a.Hq);
-      M[k] = max_s[g];
+      M[k] = max_s[gg[k]];
       // a row with no attended position in any shard (a query before the
       // first cached position) stays zero
-      zero[k] = zero_s[g] != 0 || M[k] == -INFINITY;
-      // (m, l) from shared memory when one block holds them all
-      ml[k] = staged ? ml_s + g * kShardBlock : a.ws_ml + row[k] * a.max_shards;
-      acc[k] = reinterpret_cast<const float4*>(a.ws_acc + row[k] * a.max_shards * D) + quad[k];
+      zero[k] = zero_s[gg[k]] != 0 || M[k] == -INFINITY;
       o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       L[k] = 0.f;
     }
@@ -130,8 +137,9 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
       for (int k = 0; k < 2; ++k)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          x[k][u] = __ldcg(acc[k] + (size_t)(s + u) * kQuads);
-          v[k][u] = staged ? ml[k][s + u] : __ldcg(ml[k] + s + u);
+          const size_t slot = slot_of(gg[k], s + u);
+          x[k][u] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad[k]);
+          v[k][u] = staged ? ml_s[gg[k] * cap + s + u] : __ldcg(a.ws_ml + slot);
         }
 #pragma unroll
       for (int k = 0; k < 2; ++k)
@@ -148,8 +156,9 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     for (; any && s < S; ++s) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const float4 x = __ldcg(acc[k] + (size_t)s * kQuads);
-        const float2 v = staged ? ml[k][s] : __ldcg(ml[k] + s);
+        const size_t slot = slot_of(gg[k], s);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad[k]);
+        const float2 v = staged ? ml_s[gg[k] * cap + s] : __ldcg(a.ws_ml + slot);
         const float c = fast_exp2(v.x - M[k]);
         L[k] = __fmaf_rn(c, v.y, L[k]);
         o[k].x = __fmaf_rn(c, x.x, o[k].x);
@@ -165,8 +174,9 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
                                             z ? 0.f : __fdiv_rn(o[k].y, l_sum));
       const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o[k].z, l_sum),
                                             z ? 0.f : __fdiv_rn(o[k].w, l_sum));
-      uint32_t* dst =
-          reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row[k] * D + 4 * quad[k]);
+      const size_t row = group_row(b, h, gg[k], a.T, a.G, a.Hq);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D +
+                                                  4 * quad[k]);
       dst[0] = lo;
       dst[1] = hi;
     }
@@ -184,7 +194,8 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
       seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T);
   grid_dependency_wait();
   merge_group<D, E>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
-                    [] { __syncthreads(); });
+                    kShardBlock, [] { __syncthreads(); },
+                    GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});
 }
 
 }  // namespace pgd

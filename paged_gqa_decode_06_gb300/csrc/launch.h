@@ -7,6 +7,7 @@
 
 #include "combine.cuh"
 #include "split_mma.cuh"
+#include "split_persistent.cuh"
 #include "split_simt.cuh"
 
 namespace pgd {
@@ -19,9 +20,15 @@ struct SplitLaunch {
   int group_pad;
   int variant;
   int dtype;
+  int persistent;   // launch the persistent kernel (at most grid.x CTAs)
+  int batch;
+  int num_sms;
   cudaStream_t stream;
 };
 
+int persist_smem_d64(int nt8);
+int persist_smem_d128(int nt8);
+int persist_smem_d256(int nt8);
 cudaError_t launch_split_d64(const SplitLaunch& L);
 cudaError_t launch_split_d128(const SplitLaunch& L);
 cudaError_t launch_split_d256(const SplitLaunch& L);
@@ -40,6 +47,9 @@ struct KvAppendArgs {
   int32_t B, Hkv, chunks, page_size, max_pages, num_pages;
 };
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t stream);
+
+// Dynamic shared memory of the persistent kernel for (head_dim, row tiles).
+int persist_smem(int head_dim, int nt8);
 
 // Resident CTAs per SM the kernels are sized for (shared-memory bound).
 int simt_ctas_per_sm(int head_dim);

@@ -60,6 +60,117 @@ __device__ __forceinline__ uint32_t swz_offset(int t, int d) {
   return (uint32_t)((d >> 6) * (kTile * 128) + t * 128 + ((((d >> 3) & 7) ^ (t & 7)) << 4));
 }
 
+// One consumer warp's 16 positions [tok0, tok0 + 16) of a staged tile:
+// scores^T = K . Q^T, the per-column causal / window mask, the online
+// softmax update and out^T += V^T . P^T.  kt points at the stage's K tile
+// (V follows at kTileBytes); [lo, hi) is the union of the columns' ranges
+// clipped to the shard, and the block must overlap it.
+template <int D, int NT8, class E>
+__device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int tok0, int lo,
+                                          int hi, const int (&col_lo)[NT8][2],
+                                          const int (&col_hi)[NT8][2],
+                                          const uint32_t (&qf)[NT8][D / 16][2], float scale_log2,
+                                          float (&acc)[D / 16][NT8][4], float (&m_run)[NT8][2],
+                                          float (&l_part)[NT8][2]) {
+  using C = MmaCfg<D>;
+  constexpr int KS = D / 16;
+  const int gid = lane >> 2;
+  const int mat = lane >> 3, mrow = lane & 7;
+  const int k_tok = 16 * warp + mrow + ((mat & 1) ? 8 : 0);  // K: matrix bit 0 -> +8 tokens
+  const int k_dof = (mat & 2) ? 8 : 0;                       // K: matrix bit 1 -> +8 dims
+  const int v_tok = 16 * warp + mrow + ((mat & 2) ? 8 : 0);  // V: matrix bit 1 -> +8 tokens
+  const int v_dof = (mat & 1) ? 8 : 0;                       // V: matrix bit 0 -> +8 dims
+  const uint32_t kbase = smem_u32(kt);
+  const uint32_t vbase = kbase + C::kTileBytes;
+  if (tok0 < lo || tok0 + 16 > hi) {
+    // rows of this block outside the range: clear their V rows so a
+    // zero weight never meets a non-finite cache value
+    uint8_t* vt = kt + C::kTileBytes;
+    for (int e = lane; e < 16 * (D / 8); e += 32) {
+      const int t = e / (D / 8), c = e % (D / 8);
+      const int tok = tok0 + t;
+      if (tok < lo || tok >= hi)
+        *reinterpret_cast<uint4*>(vt + swz_offset(16 * warp + t, c * 8)) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+  // scores^T = K . Q^T
+  float sc[NT8][4];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t af[4];
+    ldmatrix_x4(af, kbase + swz_offset(k_tok, ks * 16 + k_dof));
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
+  }
+  // online softmax over this block's 16 positions
+  const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
+  uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
+  bool rescale = false;
+  float alpha[NT8][2];
+#pragma unroll
+  for (int j = 0; j < NT8; ++j) {
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = (e < 2) ? tok_a : tok_b;
+      const bool ok = tok >= col_lo[j][e & 1] && tok < col_hi[j][e & 1];
+      sc[j][e] = ok ? sc[j][e] * scale_log2 : -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mx = fmaxf(sc[j][e], sc[j][e + 2]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[j][e], mx);
+      alpha[j][e] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run[j][e] - m_new);
+      rescale |= alpha[j][e] != 1.f;
+      p[e] = (sc[j][e] == -INFINITY) ? 0.f : fast_exp2(sc[j][e] - m_new);
+      p[e + 2] = (sc[j][e + 2] == -INFINITY) ? 0.f : fast_exp2(sc[j][e + 2] - m_new);
+      l_part[j][e] = l_part[j][e] * alpha[j][e] + p[e] + p[e + 2];
+      m_run[j][e] = m_new;
+    }
+    // P^T operand: fp16 head and fp16 remainder, transposed by movmatrix
+    const uint32_t h0 = ElemOps<E>::pack2(p[0], p[1]);
+    const uint32_t h1 = ElemOps<E>::pack2(p[2], p[3]);
+    const float2 f0 = ElemOps<E>::unpack2(h0);
+    const float2 f1 = ElemOps<E>::unpack2(h1);
+    const uint32_t l0 = ElemOps<E>::pack2(p[0] - f0.x, p[1] - f0.y);
+    const uint32_t l1 = ElemOps<E>::pack2(p[2] - f1.x, p[3] - f1.y);
+    pb_hi[j][0] = movmatrix_trans(h0);
+    pb_hi[j][1] = movmatrix_trans(h1);
+    pb_lo[j][0] = movmatrix_trans(l0);
+    pb_lo[j][1] = movmatrix_trans(l1);
+  }
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) {
+        acc[mi][j][0] *= alpha[j][0];
+        acc[mi][j][1] *= alpha[j][1];
+        acc[mi][j][2] *= alpha[j][0];
+        acc[mi][j][3] *= alpha[j][1];
+      }
+  }
+  // out^T += V^T . P^T
+#pragma unroll
+  for (int mi = 0; mi < KS; ++mi) {
+    uint32_t af[4];
+    ldmatrix_x4_trans(af, vbase + swz_offset(v_tok, mi * 16 + v_dof));
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      ElemOps<E>::mma(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
+      ElemOps<E>::mma(acc[mi][j], af, pb_lo[j][0], pb_lo[j][1]);
+    }
+  }
+}
+
 template <int D, int NT8, class E>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -221,13 +332,6 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     l_part[j][0] = l_part[j][1] = 0.f;
   }
 
-  // per-lane ldmatrix row offsets (the tile's token rows of this warp)
-  const int mat = lane >> 3, mrow = lane & 7;
-  const int k_tok = 16 * warp + mrow + ((mat & 1) ? 8 : 0);  // K: matrix bit 0 -> +8 tokens
-  const int k_dof = (mat & 2) ? 8 : 0;                       // K: matrix bit 1 -> +8 dims
-  const int v_tok = 16 * warp + mrow + ((mat & 2) ? 8 : 0);  // V: matrix bit 1 -> +8 tokens
-  const int v_dof = (mat & 1) ? 8 : 0;                       // V: matrix bit 0 -> +8 dims
-
   for (int i = 0; i < n_tiles && !bad; ++i) {
     const int st = i % C::kStages;
     if (!mbar_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1)) {
@@ -237,98 +341,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     }
     if (abort_s) break;
     const int tok0 = shard_lo + i * kTile + 16 * warp;  // this warp's 16 positions
-    if (tok0 + 16 > lo && tok0 < hi) {
-      uint8_t* kt = ring + st * C::kStageBytes;
-      const uint32_t kbase = smem_u32(kt);
-      const uint32_t vbase = kbase + C::kTileBytes;
-      if (tok0 < lo || tok0 + 16 > hi) {
-        // rows of this block outside the range: clear their V rows so a
-        // zero weight never meets a non-finite cache value
-        uint8_t* vt = kt + C::kTileBytes;
-        for (int e = lane; e < 16 * (D / 8); e += 32) {
-          const int t = e / (D / 8), c = e % (D / 8);
-          const int tok = tok0 + t;
-          if (tok < lo || tok >= hi)
-            *reinterpret_cast<uint4*>(vt + swz_offset(16 * warp + t, c * 8)) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      // scores^T = K . Q^T
-      float sc[NT8][4];
-#pragma unroll
-      for (int j = 0; j < NT8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t af[4];
-        ldmatrix_x4(af, kbase + swz_offset(k_tok, ks * 16 + k_dof));
-#pragma unroll
-        for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
-      }
-      // online softmax over this block's 16 positions
-      const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
-      uint32_t pb_hi[NT8][2], pb_lo[NT8][2];
-      bool rescale = false;
-      float alpha[NT8][2];
-#pragma unroll
-      for (int j = 0; j < NT8; ++j) {
-        float p[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = (e < 2) ? tok_a : tok_b;
-          const bool ok = tok >= col_lo[j][e & 1] && tok < col_hi[j][e & 1];
-          sc[j][e] = ok ? sc[j][e] * a.scale_log2 : -INFINITY;
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float mx = fmaxf(sc[j][e], sc[j][e + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_new = fmaxf(m_run[j][e], mx);
-          alpha[j][e] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_run[j][e] - m_new);
-          rescale |= alpha[j][e] != 1.f;
-          p[e] = (sc[j][e] == -INFINITY) ? 0.f : fast_exp2(sc[j][e] - m_new);
-          p[e + 2] = (sc[j][e + 2] == -INFINITY) ? 0.f : fast_exp2(sc[j][e + 2] - m_new);
-          l_part[j][e] = l_part[j][e] * alpha[j][e] + p[e] + p[e + 2];
-          m_run[j][e] = m_new;
-        }
-        // P^T operand: fp16 head and fp16 remainder, transposed by movmatrix
-        const uint32_t h0 = ElemOps<E>::pack2(p[0], p[1]);
-        const uint32_t h1 = ElemOps<E>::pack2(p[2], p[3]);
-        const float2 f0 = ElemOps<E>::unpack2(h0);
-        const float2 f1 = ElemOps<E>::unpack2(h1);
-        const uint32_t l0 = ElemOps<E>::pack2(p[0] - f0.x, p[1] - f0.y);
-        const uint32_t l1 = ElemOps<E>::pack2(p[2] - f1.x, p[3] - f1.y);
-        pb_hi[j][0] = movmatrix_trans(h0);
-        pb_hi[j][1] = movmatrix_trans(h1);
-        pb_lo[j][0] = movmatrix_trans(l0);
-        pb_lo[j][1] = movmatrix_trans(l1);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int mi = 0; mi < KS; ++mi)
-#pragma unroll
-          for (int j = 0; j < NT8; ++j) {
-            acc[mi][j][0] *= alpha[j][0];
-            acc[mi][j][1] *= alpha[j][1];
-            acc[mi][j][2] *= alpha[j][0];
-            acc[mi][j][3] *= alpha[j][1];
-          }
-      }
-      // out^T += V^T . P^T
-#pragma unroll
-      for (int mi = 0; mi < KS; ++mi) {
-        uint32_t af[4];
-        ldmatrix_x4_trans(af, vbase + swz_offset(v_tok, mi * 16 + v_dof));
-#pragma unroll
-        for (int j = 0; j < NT8; ++j) {
-          ElemOps<E>::mma(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
-          ElemOps<E>::mma(acc[mi][j], af, pb_lo[j][0], pb_lo[j][1]);
-        }
-      }
-    }
+    if (tok0 + 16 > lo && tok0 < hi)
+      mma_block<D, NT8, E>(ring + st * C::kStageBytes, warp, lane, tok0, lo, hi, col_lo, col_hi,
+                           qf, a.scale_log2, acc, m_run, l_part);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }

@@ -168,8 +168,9 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   c.window = a.window;
   c.chunk = a.chunk;
   c.max_shards = a.max_shards;
-  merge_group<D, E>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem,
-                    [nthreads] { named_barrier_sync(1, nthreads); });
+  merge_group<D, E>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem, kShardBlock,
+                    [nthreads] { named_barrier_sync(1, nthreads); },
+                    GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});
   if (threadIdx.x == 0) *ticket = 0;
 }
 

@@ -59,8 +59,9 @@ extern "C" int decode_attn_static_scratch(const decode_attn_params* p, const voi
                                           const int32_t* page_table, const int32_t* seq_lens,
                                           void* out, int32_t* err_flag, void* stream) {
   decode_attn_plan plan;
-  // argument errors first, without touching the device
-  int st = decode_attn_make_plan(p, 1, &plan);
+  // argument errors first, without touching the device (an SM count large
+  // enough that no schedule is refused for it; the real plan follows)
+  int st = decode_attn_make_plan(p, 1 << 16, &plan);
   if (st) return st;
   int device = 0, sms = 0;
   if (cudaGetDevice(&device) != cudaSuccess ||

@@ -175,6 +175,13 @@ def make(name: str, device="cpu", dtype=torch.float16) -> Workload:
         return make_custom("batched", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128,
                            page_size=16, seq_lens=L, seed=3, decoy_pages=need // 10,
                            max_pages=512, device=device, dtype=dtype)
+    if name == "many_short":  # many short sequences of mixed lengths
+        g = torch.Generator()
+        g.manual_seed(6)
+        L = torch.randint(1, 513, (1000,), generator=g, dtype=torch.int64)
+        return make_custom("many_short", batch=1000, num_q_heads=32, num_kv_heads=8,
+                           head_dim=128, page_size=16, seq_lens=L, seed=6, device=device,
+                           dtype=dtype)
     if name.startswith("ctx"):  # e.g. "ctx300_d128": short-context sweep point
         ctx, shape = name[3:].split("_")
         return make_custom(name, batch=1, page_size=16, seq_lens=[int(ctx)], seed=5,

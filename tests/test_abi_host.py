@@ -55,7 +55,8 @@ def test_library_needs_no_driver_at_load(pkg):
 def params(pkg, **kw):
     base = dict(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                 max_pages_per_seq=192, num_pages=256, max_seq_len=3060, scale=0.088,
-                window=0, variant=0, split_min=0, force_chunk=0, num_queries=1, dtype=0)
+                window=0, variant=0, split_min=0, force_chunk=0, num_queries=1, dtype=0,
+                schedule=0)
     base.update(kw)
     return pkg.DecodeAttnParams(**base)
 
@@ -109,7 +110,7 @@ def test_threshold_at_256(pkg):
 def test_large_work_targets_about_1_7_waves(pkg):
     # B=4, Hkv=8, 131072 tokens, D=128: 32 (b, h) units on 152 SMs x 2 CTAs
     p = params(pkg, batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
-               max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072)
+               max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072, schedule=1)
     plan = pkg.decode_attn_make_plan(p, 152)
     slots = 152 * plan.ctas_per_sm
     ctas = plan.grid_x * plan.grid_y * plan.grid_z
@@ -122,7 +123,8 @@ def test_large_work_targets_about_1_7_waves(pkg):
 def test_mixed_lengths_get_bounded_chunks(pkg):
     # B=64 lengths up to 8192: chunks of at most 2048 tokens keep the pieces
     # of short and long sequences balanced
-    p = params(pkg, batch=64, max_pages_per_seq=512, num_pages=18000, max_seq_len=8192)
+    p = params(pkg, batch=64, max_pages_per_seq=512, num_pages=18000, max_seq_len=8192,
+               schedule=1)
     plan = pkg.decode_attn_make_plan(p, 152)
     assert plan.chunk_tokens <= 2048 and plan.max_shards >= 4
 
@@ -167,7 +169,8 @@ def test_plan_covers_every_length(pkg, max_len, units):
     B, Hkv = units
     PS = 16
     p = params(pkg, batch=B, num_kv_heads=Hkv, num_q_heads=Hkv * 4,
-               max_pages_per_seq=(max_len + PS - 1) // PS, num_pages=10, max_seq_len=max_len)
+               max_pages_per_seq=(max_len + PS - 1) // PS, num_pages=10, max_seq_len=max_len,
+               schedule=1)
     plan = pkg.decode_attn_make_plan(p, 152)
     assert plan.chunk_tokens % 64 == 0
     assert plan.chunk_tokens * plan.max_shards >= max_len
@@ -241,3 +244,23 @@ def test_bf16_plans(pkg):
     for bad in (dict(dtype=1, variant=1), dict(dtype=2)):
         with pytest.raises(pkg.DecodeAttnError):
             pkg.decode_attn_make_plan(params(pkg, **bad), 152)
+
+
+def test_persistent_plans(pkg):
+    long_p = dict(batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
+                  max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072)
+    assert pkg.decode_attn_make_plan(params(pkg, **long_p), 152).persistent == 0  # auto: grid
+    plan = pkg.decode_attn_make_plan(params(pkg, **long_p, schedule=2), 152)
+    assert plan.persistent == 1 and plan.grid_x == 152 * plan.ctas_per_sm
+    assert plan.grid_y == plan.grid_z == 1 and plan.ctas_per_sm == 2
+    rows = plan.grid_x * 2 * 8  # two partial slots of G rows per CTA
+    assert plan.workspace_bytes >= 65536 + rows * (128 + 2) * 4
+    # the CUDA-core variant cannot run it
+    with pytest.raises(pkg.DecodeAttnError):
+        pkg.decode_attn_make_plan(params(pkg, **long_p, variant=1, schedule=2), 152)
+    # small work stays on the grid unless asked
+    assert pkg.decode_attn_make_plan(params(pkg), 152).persistent == 0
+    assert pkg.decode_attn_make_plan(params(pkg, schedule=2), 152).persistent == 1
+    with pytest.raises(pkg.DecodeAttnError) as e:
+        pkg.decode_attn_make_plan(params(pkg, batch=1025, schedule=2), 152)
+    assert e.value.code == -10
