@@ -117,7 +117,7 @@ typedef struct decode_attn_plan {
   int32_t tile_tokens;       /* tokens per pipeline stage (64) */
   int32_t chunk_tokens;      /* C: tokens per shard, a multiple of tile_tokens */
   int32_t max_shards;        /* S_max: shards of the longest planned sequence */
-  int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (shard, kv head, batch) */
+  int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (kv head, shard, batch) */
   int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
   int32_t persistent;        /* 1: persistent balanced schedule (grid_x = CTAs, slots
                                 of 2 partials per CTA); 0: grid schedule */

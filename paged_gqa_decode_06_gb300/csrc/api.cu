@@ -227,8 +227,8 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->chunk_tokens = (int32_t)chunk;
   plan->max_shards = (int32_t)max_shards;
   plan->split = max_shards > 1 ? 1 : 0;
-  plan->grid_x = (int32_t)max_shards;
-  plan->grid_y = p->num_kv_heads;
+  plan->grid_x = p->num_kv_heads;
+  plan->grid_y = (int32_t)max_shards;
   plan->grid_z = p->batch;
   plan->ctas_per_sm = ctas_per_sm;
   if (plan->split) {

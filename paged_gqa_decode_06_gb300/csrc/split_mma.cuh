@@ -191,7 +191,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   // the combine launched after this grid may be scheduled now; it waits for
   // this grid's partials with griddepcontrol.wait before reading them
   grid_launch_dependents();
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // head fastest: the Hkv CTAs of one (sequence, shard) start together and
+  // read the rows of the same positions (adjacent in the pool) side by side
+  const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
                                a.max_shards, a.T);
