@@ -188,8 +188,12 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   __shared__ int32_t bad_s;
   __shared__ volatile int32_t abort_s;
 
-  // the combine launched after this grid may be scheduled now; it waits for
-  // this grid's partials with griddepcontrol.wait before reading them
+  // launched as a programmatic dependent of the preceding kernel: its CTAs
+  // may become resident while that kernel drains, but nothing is read or
+  // written before it has completed
+  grid_dependency_wait();
+  // a kernel launched after this one (a combine, the next step) may be
+  // scheduled now; it waits the same way before touching memory
   grid_launch_dependents();
   // head fastest: the Hkv CTAs of one (sequence, shard) start together and
   // read the rows of the same positions (adjacent in the pool) side by side

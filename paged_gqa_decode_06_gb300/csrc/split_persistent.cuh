@@ -134,6 +134,10 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   __shared__ int is_last_s;
   __shared__ volatile int32_t abort_s;
 
+  // launched as a programmatic dependent: nothing is read or written before
+  // the preceding grid on the stream has completed
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int capacity = a.max_pages * a.page_size;
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
