@@ -117,10 +117,12 @@ typedef struct decode_attn_plan {
   int32_t tile_tokens;       /* tokens per pipeline stage (64) */
   int32_t chunk_tokens;      /* C: tokens per shard, a multiple of tile_tokens */
   int32_t max_shards;        /* S_max: shards of the longest planned sequence */
-  int32_t grid_x, grid_y, grid_z;  /* split-kernel grid (kv head, shard, batch) */
+  int32_t grid_x, grid_y, grid_z;  /* split-kernel grid: (kv head, shard, batch) when
+                                      head_fastest, else (shard, kv head, batch) */
   int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
   int32_t persistent;        /* 1: persistent balanced schedule (grid_x = CTAs, slots
                                 of 2 partials per CTA); 0: grid schedule */
+  int32_t head_fastest;      /* grid schedule order: 1 for plans of several waves */
   size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;

@@ -227,8 +227,13 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->chunk_tokens = (int32_t)chunk;
   plan->max_shards = (int32_t)max_shards;
   plan->split = max_shards > 1 ? 1 : 0;
-  plan->grid_x = p->num_kv_heads;
-  plan->grid_y = (int32_t)max_shards;
+  // several waves of CTAs: heads fastest; one wave: shards fastest (measured
+  // on GB300: long context 303.0 vs 307.6 us, Llama-3.1-8B shape 18.1 vs 17.5 us)
+  const int64_t slots_all = (int64_t)num_sms * ctas_per_sm;
+  const bool head_fastest = (int64_t)p->batch * p->num_kv_heads * max_shards > slots_all;
+  plan->head_fastest = head_fastest ? 1 : 0;
+  plan->grid_x = head_fastest ? p->num_kv_heads : (int32_t)max_shards;
+  plan->grid_y = head_fastest ? (int32_t)max_shards : p->num_kv_heads;
   plan->grid_z = p->batch;
   plan->ctas_per_sm = ctas_per_sm;
   if (plan->split) {
@@ -383,6 +388,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.max_shards = plan.max_shards;
   a.split = plan.split;
   a.T = num_queries(p);
+  a.head_fastest = plan.head_fastest;
   a.scale_log2 = p->scale * kLog2e;
   L.grid = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
   L.group_pad = plan.group_pad;

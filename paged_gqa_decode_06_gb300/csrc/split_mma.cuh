@@ -195,9 +195,13 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   // a kernel launched after this one (a combine, the next step) may be
   // scheduled now; it waits the same way before touching memory
   grid_launch_dependents();
-  // head fastest: the Hkv CTAs of one (sequence, shard) start together and
-  // read the rows of the same positions (adjacent in the pool) side by side
-  const int h = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+  // grid order: head fastest for plans of several waves (the Hkv CTAs of one
+  // (sequence, shard) start together and read the rows of the same positions,
+  // adjacent in the pool, side by side), shard fastest for one-wave plans
+  // (a group's shards run on neighbouring SMs for its merge)
+  const int h = a.head_fastest ? blockIdx.x : blockIdx.y;
+  const int s = a.head_fastest ? blockIdx.y : blockIdx.x;
+  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
                                a.max_shards, a.T);

@@ -175,7 +175,13 @@ def test_plan_covers_every_length(pkg, max_len, units):
     assert plan.chunk_tokens % 64 == 0
     assert plan.chunk_tokens * plan.max_shards >= max_len
     assert plan.chunk_tokens <= 1024 * min(PS, 64)   # page ids of one shard fit in smem
-    assert plan.grid_x == Hkv and plan.grid_y == plan.max_shards and plan.grid_z == B
+    if plan.head_fastest:
+        assert plan.grid_x == Hkv and plan.grid_y == plan.max_shards
+    else:
+        assert plan.grid_x == plan.max_shards and plan.grid_y == Hkv
+    assert plan.grid_z == B
+    slots = 152 * plan.ctas_per_sm
+    assert bool(plan.head_fastest) == (B * Hkv * plan.max_shards > slots)
 
 
 def declared_arity():
