@@ -20,6 +20,12 @@ constexpr int kMaxDevices = 64;
 constexpr int kMinChunk = 128;        // shortest shard the planner picks, tokens
 constexpr int kLargeChunkCap = 2048;  // longest shard for large work, unless span / 16
 constexpr int kSmemPerSm = 228 * 1024;
+// Cost model of a one-wave split plan, calibrated on GB300 chunk sweeps (one,
+// two and four sequences of 16 Ki..128 Ki tokens, the Llama-3.1-8B shape, the
+// windowed long case):
+constexpr double kStreamBytesPerS = 7.0e12;  // sustained K/V read rate of the split kernel
+constexpr double kRoundTripS = 2.0e-6;       // loaded latency: a CTA moves its ring once per trip
+constexpr double kMergeStepS = 1.2e-6;       // the last CTA's merge: one L2 round trip per 8 shards
 
 std::atomic<int> g_sm_count[kMaxDevices];
 
@@ -101,6 +107,39 @@ int persist_smem(int head_dim, int nt8) {
     default: return persist_smem_d256(nt8);
   }
 }
+// Shards per sequence for plans whose grid fits in one wave of CTA slots
+// (units = sequences x KV heads below the slot count): the S minimising
+//   t(S) = bytes / min(stream rate, units * S * ring bytes / round trip)
+//          + merge step * ceil(S / 8)          (no merge for S = 1)
+// over chunks of kMinChunk..max_chunk tokens, at most `slots` CTAs; ties go
+// to more CTAs.  Against the chunk sweeps it picks the measured best or a
+// plan within 1 % of it (one 131072-token sequence: 24 shards, 91.1 us, where
+// 1.7 waves took 102.7 us; the Llama shape: 16 shards, 16.5 against 18.5 us).
+int64_t one_wave_shards(int64_t units, int64_t slots, int64_t span, int head_dim,
+                        int64_t max_chunk) {
+  const int stages = head_dim == 64 ? 6 : 3;
+  const double ring = (double)stages * 2 * kTile * head_dim * 2;  // K + V tiles in flight
+  const double cta_rate = ring / kRoundTripS;
+  const double bytes = (double)units * (double)span * 4.0 * head_dim;
+  const int64_t s_lo = std::max<int64_t>(1, ceil_div(span, max_chunk));
+  const int64_t s_hi =
+      std::max<int64_t>(s_lo, std::min<int64_t>(slots / units, ceil_div(span, kMinChunk)));
+  int64_t best = s_lo;
+  double best_t = 1e300;
+  for (int64_t S = s_lo; S <= s_hi; ++S) {
+    const int64_t chunk = round_up(ceil_div(span, S), kTile);
+    if (chunk > max_chunk) continue;
+    const int64_t se = ceil_div(span, chunk);  // shards this chunk really gives
+    const double rate = std::min(kStreamBytesPerS, (double)(units * se) * cta_rate);
+    const double t = bytes / rate + (se > 1 ? kMergeStepS * (double)ceil_div(se, 8) : 0.0);
+    if (t < best_t * (1.0 - 1e-3) || (t <= best_t * (1.0 + 1e-3) && se > best)) {
+      best = se;
+      best_t = std::min(best_t, t);
+    }
+  }
+  return best;
+}
+
 int simt_ctas_per_sm(int head_dim) {
   // dynamic ring + static smem (page coordinates, barriers, scratch) + 1 KB
   const size_t per_cta = simt_smem_bytes(head_dim) + kMaxPieces * 4 + 2048 + 1024;
@@ -156,9 +195,9 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
     // Shard count from the work bound (every (sequence, KV head) unit at the
     // longest length) and the CTA slots (SMs x resident CTAs), calibrated on
     // GB300 sweeps of the chunk size:
-    //  * small work (up to 1 MiB per slot): one wave, as many shards as fit,
-    //    chunks of at least 128 tokens -- a second wave costs a second
-    //    prologue (length, page ids, first TMA round trip) on a short step;
+    //  * fewer units than slots: one wave, the shard count from the cost
+    //    model above (stream rate against the merge's serial tail);
+    //  * small work otherwise (up to 1 MiB per slot): one shard per unit;
     //  * large work: about 1.7 waves of CTAs, fewer prologues while DRAM stays
     //    saturated to the end; chunks capped at max(2048, span / 16) tokens
     //    so that batches of mixed lengths still cut into balanced pieces.
@@ -166,7 +205,9 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
     const int64_t slots = (int64_t)num_sms * ctas_per_sm;
     const int64_t work_bytes = units * span * 4 * p->head_dim;
     int64_t S;
-    if (work_bytes <= slots * (int64_t(1) << 20)) {
+    if (units < slots) {
+      S = one_wave_shards(units, slots, span, p->head_dim, max_chunk);
+    } else if (work_bytes <= slots * (int64_t(1) << 20)) {
       S = std::max<int64_t>(1, std::min(slots / units, ceil_div(span, kMinChunk)));
     } else {
       const int64_t target = std::max<int64_t>(1, (17 * slots + 5 * units) / (10 * units));

@@ -182,6 +182,11 @@ def make(name: str, device="cpu", dtype=torch.float16) -> Workload:
         return make_custom("many_short", batch=1000, num_q_heads=32, num_kv_heads=8,
                            head_dim=128, page_size=16, seq_lens=L, seed=6, device=device,
                            dtype=dtype)
+    if name.startswith("seq"):  # e.g. "seq32768" or "seq65536x2": long-case shape, B x L
+        L, _, B = name[3:].partition("x")
+        return make_custom(name, batch=int(B or 1), num_q_heads=64, num_kv_heads=8,
+                           head_dim=128, page_size=64, seq_lens=[int(L)] * int(B or 1), seed=7,
+                           device=device, dtype=dtype)
     if name.startswith("ctx"):  # e.g. "ctx300_d128": short-context sweep point
         ctx, shape = name[3:].split("_")
         return make_custom(name, batch=1, page_size=16, seq_lens=[int(ctx)], seed=5,

@@ -107,8 +107,11 @@ def test_threshold_at_256(pkg):
     assert plan.split == 0
 
 
-def test_large_work_targets_about_1_7_waves(pkg):
-    # B=4, Hkv=8, 131072 tokens, D=128: 32 (b, h) units on 152 SMs x 2 CTAs
+def test_few_units_take_one_wave(pkg):
+    # B=4, Hkv=8, 131072 tokens, D=128: 32 (b, h) units on 152 SMs x 2 CTAs.
+    # Fewer units than slots: one wave, shard count from the cost model
+    # (stream rate against one merge round trip per 8 shards): 8 shards, 256
+    # CTAs (the chunk sweep's best; 1.7 waves and 1.26 waves measured slower)
     p = params(pkg, batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
                max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072, schedule=1)
     plan = pkg.decode_attn_make_plan(p, 152)
@@ -116,8 +119,41 @@ def test_large_work_targets_about_1_7_waves(pkg):
     ctas = plan.grid_x * plan.grid_y * plan.grid_z
     assert plan.split == 1
     assert plan.chunk_tokens * plan.max_shards >= 131072
-    assert 1.5 * slots <= ctas <= 1.9 * slots, (ctas, slots)
+    assert plan.max_shards == 8 and ctas == 256 and ctas <= slots, (ctas, slots)
     assert plan.workspace_bytes >= 64 * 1024 + 4 * 64 * plan.max_shards * (128 + 2) * 4
+
+
+@pytest.mark.parametrize("batch,max_len,shards", [
+    (1, 131072, 24),   # one long sequence: 192 CTAs
+    (1, 16384, 16),    # 128 CTAs: the merge tail outweighs more streaming CTAs
+    (2, 65536, 16),    # 256 CTAs
+    (4, 32768, 8),     # 256 CTAs
+])
+def test_one_wave_cost_model_picks(pkg, batch, max_len, shards):
+    # the picks the model makes on the chunk sweep's shapes (64/8 heads,
+    # D=128, page 64), each the measured best or within 1 % of it
+    p = params(pkg, batch=batch, num_q_heads=64, num_kv_heads=8, page_size=64,
+               max_pages_per_seq=max_len // 64, num_pages=batch * max_len // 64,
+               max_seq_len=max_len, schedule=1)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    assert plan.max_shards == shards
+    assert plan.grid_x * plan.grid_y * plan.grid_z <= 152 * plan.ctas_per_sm
+    assert plan.head_fastest == 0
+
+
+def test_one_wave_plan_never_exceeds_the_slots(pkg):
+    for B in (1, 2, 3, 5, 7, 9, 16, 37):
+        for L in (300, 1000, 3060, 20000, 131072):
+            p = params(pkg, batch=B, max_pages_per_seq=(L + 15) // 16, num_pages=10,
+                       max_seq_len=L, schedule=1)
+            plan = pkg.decode_attn_make_plan(p, 152)
+            ctas = plan.grid_x * plan.grid_y * plan.grid_z
+            if B * 8 < 152 * plan.ctas_per_sm:
+                # unless the shard's page ids (1024 per shard, page 16) force
+                # more shards
+                assert ctas <= 152 * plan.ctas_per_sm or \
+                    plan.max_shards == math.ceil(L / (1024 * 16)), (B, L, ctas)
+                assert plan.chunk_tokens >= 128 or plan.max_shards == 1
 
 
 def test_mixed_lengths_get_bounded_chunks(pkg):
