@@ -185,6 +185,8 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
   __shared__ int32_t coord_s[kMaxPieces];
   __shared__ float2 ml_s[kWarps][GP];
+  __shared__ float cw_s[kWarps][GP];  // each warp's weight per row
+  __shared__ float2 row_s[GP];        // (M, L) per row
   __shared__ int32_t bad_s;
   __shared__ volatile int32_t abort_s;
 
@@ -370,7 +372,11 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       l_part[j][e] = l;
     }
   named_barrier_sync(1, kWarps * 32);  // every consumer is done with the ring
-  float* acc_s = reinterpret_cast<float*>(ring);  // [kWarps][GP][D]
+  // the warps' states in [kWarps][GP][D + 4] fp32: the padding sends a
+  // fragment's 32 stores to 32 distinct banks and keeps rows 16-byte aligned
+  constexpr int kRowStride = D + 4;
+  static_assert(kWarps * GP * kRowStride * 4 <= C::kRingBytes, "warp states fit in the ring");
+  float* acc_s = reinterpret_cast<float*>(ring);
   if (gid == 0) {
 #pragma unroll
     for (int j = 0; j < NT8; ++j)
@@ -383,37 +389,65 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
 #pragma unroll
     for (int j = 0; j < NT8; ++j) {
       const int hd = 8 * j + 2 * tig, d = 16 * mi + gid;
-      float* base = acc_s + (warp * GP) * D;
-      base[hd * D + d] = acc[mi][j][0];
-      base[(hd + 1) * D + d] = acc[mi][j][1];
-      base[hd * D + d + 8] = acc[mi][j][2];
-      base[(hd + 1) * D + d + 8] = acc[mi][j][3];
+      float* base = acc_s + (warp * GP) * kRowStride;
+      base[hd * kRowStride + d] = acc[mi][j][0];
+      base[(hd + 1) * kRowStride + d] = acc[mi][j][1];
+      base[hd * kRowStride + d + 8] = acc[mi][j][2];
+      base[(hd + 1) * kRowStride + d + 8] = acc[mi][j][3];
     }
   named_barrier_sync(1, kWarps * 32);
-  const bool dead = bad || abort_s != 0;
-
-  for (int e = threadIdx.x; e < R * D; e += kWarps * 32) {
-    const int g = e / D, d = e % D;
+  // per row: M = max over warps, each warp's weight c_w = 2^(m_w - M) (none
+  // for a warp that saw no position of the row), L = sum_w c_w l_w in warp
+  // order
+  if (threadIdx.x < R) {
+    const int g = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml_s[w][g].x);
-    float L = 0.f, O = 0.f;
+    float L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const float2 ml = ml_s[w][g];
-      if (ml.y == 0.f) continue;
-      const float c = fast_exp2(ml.x - M);
-      L += c * ml.y;
-      O += c * acc_s[(w * GP + g) * D + d];
+      const float c = ml.y == 0.f ? 0.f : fast_exp2(ml.x - M);
+      if (ml.y != 0.f) L += c * ml.y;
+      cw_s[w][g] = ml.y == 0.f ? 0.f : c;
+    }
+    row_s[g] = make_float2(M, L);
+  }
+  named_barrier_sync(1, kWarps * 32);
+  const bool dead = bad || abort_s != 0;
+
+  // fold the warps, 4 dims per thread and pass, in warp order
+  constexpr int kQuads = D / 4;
+  for (int e = threadIdx.x; e < R * kQuads; e += kWarps * 32) {
+    const int g = e / kQuads, q = e % kQuads;
+    const float2 ML = row_s[g];
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float c = cw_s[w][g];
+      if (c == 0.f) continue;
+      const float4 x =
+          *reinterpret_cast<const float4*>(acc_s + (w * GP + g) * kRowStride + 4 * q);
+      O.x += c * x.x;
+      O.y += c * x.y;
+      O.z += c * x.z;
+      O.w += c * x.w;
     }
     const size_t row = group_row(b, h, g, a.T, G, a.Hq);
     if (!a.split) {
-      static_cast<uint16_t*>(a.out)[row * D + d] =
-          ElemOps<E>::round((dead || L == 0.f) ? 0.f : O / L);
+      const bool z = dead || ML.y == 0.f;
+      const uint32_t lo = (uint32_t)ElemOps<E>::round(z ? 0.f : O.x / ML.y) |
+                          ((uint32_t)ElemOps<E>::round(z ? 0.f : O.y / ML.y) << 16);
+      const uint32_t hi = (uint32_t)ElemOps<E>::round(z ? 0.f : O.z / ML.y) |
+                          ((uint32_t)ElemOps<E>::round(z ? 0.f : O.w / ML.y) << 16);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + row * D + 4 * q) =
+          make_uint2(lo, hi);
     } else {
       const size_t slot = row * a.max_shards + s;
-      a.ws_acc[slot * D + d] = dead ? 0.f : O;
-      if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
+      *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) =
+          dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
+      if (q == 0) a.ws_ml[slot] = make_float2(ML.x, dead ? -1.f : ML.y);
     }
   }
   if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
