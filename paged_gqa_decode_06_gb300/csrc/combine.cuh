@@ -58,6 +58,32 @@ struct GridSlots {
   }
 };
 
+// U consecutive shards [s, s + U) of one output item (row g, dims 4*quad ..
+// 4*quad + 3): the U accumulator loads (and (m, l) reads) first, then the
+// fused multiply-adds in shard order.
+template <int D, int U, class SlotOf>
+__device__ __forceinline__ void merge_batch(const CombineArgs& a, int g, int quad, int s, float M,
+                                            bool staged, const float2* ml_s, int cap,
+                                            SlotOf slot_of, float4& o, float& L) {
+  float4 x[U];
+  float2 v[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const size_t slot = slot_of(g, s + u);
+    x[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad);
+    v[u] = staged ? ml_s[g * cap + s + u] : __ldcg(a.ws_ml + slot);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float c = fast_exp2(v[u].x - M);
+    L = __fmaf_rn(c, v[u].y, L);
+    o.x = __fmaf_rn(c, x[u].x, o.x);
+    o.y = __fmaf_rn(c, x[u].y, o.y);
+    o.z = __fmaf_rn(c, x[u].z, o.z);
+    o.w = __fmaf_rn(c, x[u].w, o.w);
+  }
+}
+
 // Merges the S shard partials of group (b, h) (its T*G query rows) into
 // out, in ascending shard order, using threads [0, nthreads) (tid = this
 // thread's index among them) and `smem` (merge_smem_bytes(rows, cap)
@@ -106,9 +132,35 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
   }
   sync();
 
+  const int total = G * kQuads;
+  if (total <= nthreads) {
+    // at most one output item (row, 4 dims) per thread: its shard loads go
+    // out 16 at a time (then 8, then one by one), so a batch of 16 shards
+    // costs one L2 round trip
+    const int e = tid;
+    if (e < total) {
+      const int g = e / kQuads, quad = e % kQuads;
+      const float M = max_s[g];
+      const bool zero = zero_s[g] != 0 || M == -INFINITY;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+      int s = 0;
+      for (; !zero && s + 16 <= S; s += 16) merge_batch<D, 16>(a, g, quad, s, M, staged, ml_s, cap, slot_of, o, L);
+      for (; !zero && s + 8 <= S; s += 8) merge_batch<D, 8>(a, g, quad, s, M, staged, ml_s, cap, slot_of, o, L);
+      for (; !zero && s < S; ++s) merge_batch<D, 1>(a, g, quad, s, M, staged, ml_s, cap, slot_of, o, L);
+      const bool z = zero || L == 0.f;
+      const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
+      const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
+      const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * quad);
+      dst[0] = lo;
+      dst[1] = hi;
+    }
+    return;
+  }
   // two output items (row, 4 dims) per thread and pass, their shard loads
   // issued together so several L2 round trips overlap
-  const int total = G * kQuads;
   for (int e0 = tid; e0 < total; e0 += 2 * nthreads) {
     int e[2] = {e0, e0 + nthreads};
     const int n_items = e[1] < total ? 2 : 1;
