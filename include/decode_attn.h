@@ -123,6 +123,9 @@ typedef struct decode_attn_plan {
   int32_t persistent;        /* 1: persistent balanced schedule (grid_x = CTAs, slots
                                 of 2 partials per CTA); 0: grid schedule */
   int32_t head_fastest;      /* grid schedule order: 1 for plans of several waves */
+  int32_t ring_stages;       /* 64-token K/V stages in flight per CTA: 3 (6 at D=64);
+                                2 (4 at D=64) for grids of several waves of short
+                                shards, which fit 3 CTAs per SM (tensor-core variant) */
   size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;

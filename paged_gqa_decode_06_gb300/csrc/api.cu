@@ -145,6 +145,16 @@ int simt_ctas_per_sm(int head_dim) {
   const size_t per_cta = simt_smem_bytes(head_dim) + kMaxPieces * 4 + 2048 + 1024;
   return std::max<int>(1, (int)(kSmemPerSm / per_cta));
 }
+int mma_ctas_per_sm(int head_dim, bool shallow) {
+  size_t ring;
+  switch (head_dim) {
+    case 64: ring = shallow ? MmaCfg<64, true>::kSmemBytes : MmaCfg<64>::kSmemBytes; break;
+    case 128: ring = shallow ? MmaCfg<128, true>::kSmemBytes : MmaCfg<128>::kSmemBytes; break;
+    default: ring = MmaCfg<256>::kSmemBytes; break;
+  }
+  const size_t per_cta = ring + kMaxPieces * 4 + 2048 + 1024;
+  return std::max<int>(1, (int)(kSmemPerSm / per_cta));
+}
 }  // namespace pgd
 
 extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sms,
@@ -253,6 +263,7 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
     plan->max_shards = 0;
     plan->split = 1;
     plan->persistent = 1;
+    plan->ring_stages = p->head_dim == 64 ? 6 : 3;
     plan->grid_x = (int32_t)nc;
     plan->grid_y = 1;
     plan->grid_z = 1;
@@ -268,15 +279,30 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->chunk_tokens = (int32_t)chunk;
   plan->max_shards = (int32_t)max_shards;
   plan->split = max_shards > 1 ? 1 : 0;
+  // Shallow ring (tensor-core kernel, D <= 128): for grids of several waves
+  // of short shards (at most 8 tiles each), 2 stages (4 at D = 64) fit 3
+  // CTAs per SM, and more CTAs' first round trips overlap.  GB300: a
+  // thousand sequences of U[1, 512] tokens 203.3 -> 178.4 us; long streams
+  // lose by it (one 131072-token sequence 88.5 -> 95.6 us), so only short
+  // shards take it.
+  const int64_t ctas = (int64_t)p->batch * p->num_kv_heads * max_shards;
+  const bool shallow = variant == DECODE_ATTN_VARIANT_MMA &&
+                       (p->head_dim == 64 || (p->head_dim == 128 && group_pad == 8)) &&
+                       chunk <= 8 * kTile && ctas > (int64_t)num_sms * ctas_per_sm;
+  int cps = ctas_per_sm;
+  if (variant == DECODE_ATTN_VARIANT_MMA) cps = mma_ctas_per_sm(p->head_dim, shallow);
+  plan->ring_stages = variant == DECODE_ATTN_VARIANT_MMA
+                          ? (p->head_dim == 64 ? (shallow ? 4 : 6) : (shallow ? 2 : 3))
+                          : (p->head_dim == 64 ? 6 : 3);
   // several waves of CTAs: heads fastest; one wave: shards fastest (measured
   // on GB300: long context 303.0 vs 307.6 us, Llama-3.1-8B shape 18.1 vs 17.5 us)
-  const int64_t slots_all = (int64_t)num_sms * ctas_per_sm;
-  const bool head_fastest = (int64_t)p->batch * p->num_kv_heads * max_shards > slots_all;
+  const int64_t slots_all = (int64_t)num_sms * cps;
+  const bool head_fastest = ctas > slots_all;
   plan->head_fastest = head_fastest ? 1 : 0;
   plan->grid_x = head_fastest ? p->num_kv_heads : (int32_t)max_shards;
   plan->grid_y = head_fastest ? (int32_t)max_shards : p->num_kv_heads;
   plan->grid_z = p->batch;
-  plan->ctas_per_sm = ctas_per_sm;
+  plan->ctas_per_sm = cps;
   if (plan->split) {
     // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
     const size_t rows = (size_t)p->batch * T * p->num_q_heads * (size_t)max_shards;
@@ -436,6 +462,10 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.variant = plan.variant;
   L.dtype = p->dtype;
   L.persistent = plan.persistent;
+  L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && !plan.persistent &&
+               p->head_dim <= 128 && plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
+                  ? 1
+                  : 0;  // the launcher has the shallow kernels the planner picks from
   L.batch = p->batch;
   L.num_sms = plan.ctas_per_sm > 0 ? plan.grid_x / plan.ctas_per_sm : plan.grid_x;
   L.stream = stream;

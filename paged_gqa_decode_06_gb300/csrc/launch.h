@@ -21,6 +21,7 @@ struct SplitLaunch {
   int variant;
   int dtype;
   int persistent;   // launch the persistent kernel (at most grid.x CTAs)
+  int shallow;      // tensor-core kernel with the shallow ring (MmaCfg kShallow)
   int batch;
   int num_sms;
   cudaStream_t stream;
@@ -53,6 +54,7 @@ int persist_smem(int head_dim, int nt8);
 
 // Resident CTAs per SM the kernels are sized for (shared-memory bound).
 int simt_ctas_per_sm(int head_dim);
+int mma_ctas_per_sm(int head_dim, bool shallow);
 size_t simt_smem_bytes(int head_dim);
 
 }  // namespace pgd

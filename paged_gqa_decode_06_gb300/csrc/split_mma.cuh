@@ -21,11 +21,14 @@
 
 namespace pgd {
 
-template <int D>
+// kShallow: the ring of plans made of many short shards, 2 stages (4 at
+// D = 64) instead of 3 (6), so that 3 CTAs fit per SM and more CTAs' first
+// round trips overlap.
+template <int D, bool kShallow = false>
 struct MmaCfg {
   static constexpr int kWarps = 4;  // consumer warps, 16 tokens of each stage apiece
   static constexpr int kThreads = (kWarps + 1) * 32;
-  static constexpr int kStages = (D == 64) ? 6 : 3;
+  static constexpr int kStages = (D == 64) ? (kShallow ? 4 : 6) : (kShallow ? 2 : 3);
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
@@ -171,11 +174,11 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
   }
 }
 
-template <int D, int NT8, class E>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads)
+template <int D, int NT8, class E, bool SH = false>
+__global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
-  using C = MmaCfg<D>;
+  using C = MmaCfg<D, SH>;
   constexpr int GP = 8 * NT8;  // padded heads of the group
   constexpr int KS = D / 16;   // k-steps of q.k, m-tiles of p.v
   constexpr int kWarps = C::kWarps;

@@ -306,3 +306,29 @@ def test_persistent_plans(pkg):
     with pytest.raises(pkg.DecodeAttnError) as e:
         pkg.decode_attn_make_plan(params(pkg, batch=1025, schedule=2), 152)
     assert e.value.code == -10
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,stages", [(128, 32, 8, 2), (64, 32, 8, 4), (64, 64, 4, 4),
+                                             (128, 64, 4, None), (256, 16, 4, None)])
+def test_shallow_ring_for_many_short_shards(pkg, D, Hq, Hkv, stages):
+    # a thousand sequences of up to 512 tokens: several waves of one-shard
+    # CTAs take the 2-stage (4 at D=64) ring and 3 CTAs per SM, except where
+    # three CTAs per SM do not fit (D=256; D=128 with 16 query rows)
+    p = params(pkg, batch=1000, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+               max_pages_per_seq=32, num_pages=40000, max_seq_len=512, schedule=1)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    assert plan.chunk_tokens <= 512
+    if stages is None:
+        assert plan.ring_stages == (6 if D == 64 else 3)
+    else:
+        assert plan.ring_stages == stages and plan.ctas_per_sm == 3
+
+
+def test_long_shards_keep_the_deep_ring(pkg):
+    for p in (params(pkg),  # Llama-3.1-8B shape: one wave
+              params(pkg, batch=64, max_pages_per_seq=512, num_pages=18000, max_seq_len=8192,
+                     schedule=1),  # batched: 2048-token shards
+              params(pkg, batch=4, num_q_heads=64, page_size=64, max_pages_per_seq=2048,
+                     num_pages=8192, max_seq_len=131072)):
+        plan = pkg.decode_attn_make_plan(p, 152)
+        assert plan.ring_stages == 3 and plan.ctas_per_sm == 2

@@ -315,14 +315,33 @@ def test_empty_batch_entry(pkg):
 
 # ---------------------------------------------------- ABI entry points
 
-def test_split_plus_combine_equals_decode_attn(pkg):
-    w = workloads.make("llama", device=DEV)
+@pytest.mark.parametrize("case", ["llama", "sweep_d256", "g8_mixed", "g8_bf16"])
+def test_split_plus_combine_equals_decode_attn(pkg, case):
+    """The standalone combine kernel re-merges the partials the split kernel
+    left and must give the fused last-CTA merge's bits.  The cases take
+    different accumulation paths in the two kernels (one output item per
+    thread in both; two per thread in the fused merge against one in the
+    combine kernel), which share the shard order and arithmetic."""
+    if case in ("llama", "sweep_d256"):
+        w = workloads.make(case, device=DEV)
+    else:
+        dt = torch.bfloat16 if case == "g8_bf16" else torch.float16
+        w = workloads.make_custom(case, batch=3, num_q_heads=64, num_kv_heads=8, head_dim=128,
+                                  page_size=16, seq_lens=[3000, 1500, 257], seed=31,
+                                  device=DEV, dtype=dt)
     ref, _ = run(pkg, w)
     out, ws = pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
                                     w.scale, max_seq_len=w.max_seq_len())
+    plan_shards = pkg.decode_attn_make_plan(
+        pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len()),
+        torch.cuda.get_device_properties(DEV).multi_processor_count).max_shards
+    assert plan_shards > 1
     params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    fused = out.clone()
+    out.zero_()
     pkg.decode_attn_combine(params, w.seq_lens, out, ws)
     torch.cuda.synchronize()
+    assert torch.equal(fused, ref)
     assert torch.equal(out, ref)
 
 
@@ -420,3 +439,36 @@ def test_dirty_workspace_is_detected_and_clearable(pkg):
                               max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0 and torch.equal(out, ref)
+
+
+# ------------------------------------------------- shallow ring (many short)
+
+@pytest.mark.parametrize("D,Hq,Hkv,dt,window", [
+    (128, 32, 8, torch.float16, 0), (128, 32, 8, torch.bfloat16, 100),
+    (64, 32, 8, torch.float16, 0), (64, 64, 4, torch.float16, 37)])
+def test_shallow_ring_parity(pkg, D, Hq, Hkv, dt, window):
+    """Several waves of one-shard CTAs (400 sequences of 0..512 tokens) run
+    the 2-stage (4 at D=64) ring, 3 CTAs per SM; against the oracle, and
+    bitwise run to run."""
+    g = torch.Generator().manual_seed(90 + D + Hq)
+    lens = torch.randint(1, 513, (400,), generator=g)
+    lens[::53] = 1
+    w = workloads.make_custom("shallow", batch=400, num_q_heads=Hq, num_kv_heads=Hkv,
+                              head_dim=D, page_size=16, seq_lens=lens, seed=91, dtype=dt,
+                              device=DEV)
+    w.seq_lens[7] = 0
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, window, 512)
+    plan = pkg.decode_attn_make_plan(params,
+                                     torch.cuda.get_device_properties(DEV).multi_processor_count)
+    assert plan.ring_stages == (4 if D == 64 else 2)
+    out, err = run(pkg, w, window=window, max_seq_len=512)
+    assert err == 0
+    ref = oracle_of(w, window=window)
+    if dt == torch.bfloat16:
+        rel, mab, rrel = compare(out, ref)
+        assert rel <= 3e-3 and mab <= 1e-2 and rrel <= 6e-3, (rel, mab, rrel)
+    else:
+        assert_parity(out, ref)
+    again, _ = run(pkg, w, window=window, max_seq_len=512)
+    assert torch.equal(out, again)
+    assert torch.all(out[7] == 0)
