@@ -74,6 +74,13 @@ def parse_args(argv=None):
                     help="0 planner, 1 grid, 2 persistent balanced")
     ap.add_argument("--eager", action="store_true",
                     help="launch each step from the host instead of replaying a CUDA graph")
+    ap.add_argument("--dump", default="",
+                    help="write the step's output (fp32), the workload and the plan to this "
+                         ".npz for offline comparison with the oracle")
+    ap.add_argument("--context-sweep", action="store_true",
+                    help="threshold A/B instead of the bench line: contexts 1..512 of the "
+                         "three head-dim shapes, split threshold 256 (default), always split, "
+                         "or single pass up to 512; one JSON line per point")
     return ap.parse_args(argv)
 
 
@@ -502,6 +509,82 @@ def gpu_arm(args):
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
+        if args.dump:
+            import numpy as np
+            np.savez(args.dump, out=out.float().cpu().numpy(), workload=args.workload,
+                     dtype=args.dtype, queries=T, append=bool(args.append),
+                     plan=json.dumps(plan.as_dict()))
+
+
+# ------------------------------------------------------------ context sweep
+
+SWEEP_CONTEXTS = (1, 2, 3, 8, 32, 64, 128, 192, 255, 256, 257, 320, 384, 448, 512)
+
+
+def context_sweep(args):
+    """Threshold A/B over short contexts (the 256-token split threshold):
+    every point is timed like the bench's small workloads (graph replay, L2
+    flushed before each step, events around it)."""
+    import torch
+    import paged_gqa_decode_06_gb300 as pkg
+    from paged_gqa_decode_06_gb300 import build, workloads
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    pkg.load_library()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush_w = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
+    K = max(10, min(args.steps, 300))
+    modes = (("threshold 256", 0), ("always split", 1), ("single pass to 512", 512))
+    summary = {}
+    for shape in ("d64", "d128", "d256"):
+        for ctx in SWEEP_CONTEXTS:
+            w = workloads.make(f"ctx{ctx}_{shape}", device=dev)
+            out = torch.empty_like(w.q)
+            for label, split_min in modes:
+                params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, ctx, 0,
+                                         split_min)
+                plan = pkg.decode_attn_make_plan(params, props.multi_processor_count)
+                ws = torch.zeros(max(pkg.decode_attn_workspace_size(params, local), 256),
+                                 dtype=torch.uint8, device=dev)
+
+                def step():
+                    pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                                    out=out, max_seq_len=ctx, workspace=ws, split_min=split_min)
+
+                for _ in range(3):
+                    step()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step()
+                evs = []
+                for _ in range(K):
+                    flush_w.zero_()
+                    flush_r.sum()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    g.replay()
+                    e1.record()
+                    evs.append((e0, e1))
+                torch.cuda.synchronize()
+                us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+                summary.setdefault(label, []).append(us)
+                print(json.dumps({"sweep": "context", "shape": shape, "context": ctx,
+                                  "mode": label, "split": plan.split,
+                                  "shards": plan.max_shards, "us_per_step_median": us,
+                                  "steps": K}), flush=True)
+                del g, ws
+    print(json.dumps({"sweep": "context", "summary_mean_us": {
+        k: statistics.mean(v) for k, v in summary.items()}, "points": len(SWEEP_CONTEXTS) * 3,
+        "l2": "flushed before every step (write of 4x L2, then read of 4x L2)"}), flush=True)
 
 
 # ------------------------------------------------------------ reference arm
@@ -548,6 +631,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         reference_arm(args)
+    elif args.context_sweep:
+        context_sweep(args)
     else:
         gpu_arm(args)
     import torch.distributed as dist

@@ -111,8 +111,9 @@ int persist_smem(int head_dim, int nt8) {
 // (units = sequences x KV heads below the slot count): the S minimising
 //   t(S) = bytes / min(stream rate, units * S * ring bytes / round trip)
 //          + merge step * ceil(S / 8)          (no merge for S = 1)
-// over chunks of kMinChunk..max_chunk tokens, at most `slots` CTAs; ties go
-// to more CTAs.  Against the chunk sweeps it picks the measured best or a
+// over chunks of kMinChunk..max_chunk tokens, at most `slots` CTAs and at
+// least two shards (the length is above the split threshold); ties go to
+// more CTAs.  Against the chunk sweeps it picks the measured best or a
 // plan within 1 % of it (one 131072-token sequence: 24 shards, 91.1 us, where
 // 1.7 waves took 102.7 us; the Llama shape: 16 shards, 16.5 against 18.5 us).
 int64_t one_wave_shards(int64_t units, int64_t slots, int64_t span, int head_dim,
@@ -121,7 +122,8 @@ int64_t one_wave_shards(int64_t units, int64_t slots, int64_t span, int head_dim
   const double ring = (double)stages * 2 * kTile * head_dim * 2;  // K + V tiles in flight
   const double cta_rate = ring / kRoundTripS;
   const double bytes = (double)units * (double)span * 4.0 * head_dim;
-  const int64_t s_lo = std::max<int64_t>(1, ceil_div(span, max_chunk));
+  // above the split threshold the step is split: at least two shards
+  const int64_t s_lo = std::max<int64_t>(2, ceil_div(span, max_chunk));
   const int64_t s_hi =
       std::max<int64_t>(s_lo, std::min<int64_t>(slots / units, ceil_div(span, kMinChunk)));
   int64_t best = s_lo;

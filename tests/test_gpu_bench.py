@@ -1,0 +1,68 @@
+"""The bench harness on a GPU: the default JSON line's contract keys, and the
+output dump (--dump) compared offline against the f64 oracle on the same
+seeded workload, the way a dumped step is checked after a run."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_gqa_decode_06_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*extra):
+    r = subprocess.run([sys.executable, "bench.py", *extra], cwd=ROOT, capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+@pytest.fixture(scope="module")
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_bench_line_and_dump_match_the_oracle(gpu, tmp_path, name):
+    path = str(tmp_path / f"{name}.npz")
+    (line,) = run_bench("--workload", name, "--steps", "5", "--warmup", "3", "--e2e-steps", "0",
+                        "--no-cpu-baseline", "--dump", path)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["steps"] == 5 and line["gpu_launches"] == 5 and line["value"] > 0
+    roof = line["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    d = np.load(path)
+    assert str(d["workload"]) == name and json.loads(str(d["plan"]))["variant"] == 2
+    # the workloads draw from the device's own generator: regenerate on the
+    # device the bench ran on, then compare on the host
+    w = workloads.make(name, device="cuda:0").to("cpu")
+    ref = oracle.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                             w.window)
+    got = d["out"].astype(np.float64).reshape(ref.shape)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= 5e-4 and np.abs(got - ref).max() <= 2e-3, rel
+
+
+def test_context_sweep_runs(gpu):
+    lines = run_bench("--context-sweep", "--steps", "10")
+    points = [l for l in lines if "context" in l]
+    assert len(points) == 15 * 3 * 3
+    for p in points:
+        assert p["us_per_step_median"] > 0
+        # the default threshold: single pass up to 256 positions, split above
+        if p["mode"] == "threshold 256" and p["context"] > 1:
+            assert p["split"] == (1 if p["context"] > 256 else 0), p
+    assert "summary_mean_us" in lines[-1]
