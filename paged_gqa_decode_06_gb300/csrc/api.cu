@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -40,6 +41,30 @@ int sm_count(int device, int* out) {
   }
   *out = n;
   return DECODE_ATTN_OK;
+}
+
+// A positive integer from the environment, read once per process (0 when
+// unset or not a positive number).
+int env_positive(const char* name) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return 0;
+  char* end = nullptr;
+  const long x = std::strtol(v, &end, 10);
+  return (end && *end == 0 && x > 0 && x < (1L << 30)) ? (int)x : 0;
+}
+int env_positive_now(const char* name) { return env_positive(name); }
+
+// Process-wide defaults for the planner's two knobs, for A/B runs without
+// code changes: DECODE_ATTN_SPLIT_MIN (the split threshold, default 256) and
+// DECODE_ATTN_FORCE_CHUNK (a fixed shard length); a nonzero field of
+// decode_attn_params takes precedence.
+int env_split_min() {
+  static const int v = env_positive("DECODE_ATTN_SPLIT_MIN");
+  return v > 0 ? v : kDefaultSplitMin;
+}
+int env_force_chunk() {
+  static const int v = env_positive("DECODE_ATTN_FORCE_CHUNK");
+  return v;
 }
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -194,12 +219,13 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   const int64_t span = std::max<int64_t>(1, p->window > 0 ? attended + kTile - 1 : max_len);
   const int box_t = std::min(p->page_size, kTile);
   const int64_t max_chunk = (int64_t)kMaxPieces * box_t;
-  const int split_min = p->split_min > 0 ? p->split_min : kDefaultSplitMin;
+  const int split_min = p->split_min > 0 ? p->split_min : env_split_min();
   const int ctas_per_sm = simt_ctas_per_sm(p->head_dim);
 
   int64_t chunk;
-  if (p->force_chunk > 0) {
-    chunk = round_up(p->force_chunk, kTile);
+  const int force_chunk = p->force_chunk > 0 ? p->force_chunk : env_force_chunk();
+  if (force_chunk > 0) {
+    chunk = round_up(force_chunk, kTile);
     if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
   } else if (attended <= split_min) {
     chunk = round_up(span, kTile);  // one shard covers the whole range
@@ -424,7 +450,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
               const int32_t* seq_lens, void* out, const Workspace& ws, int32_t* err_flag,
               cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
   if (p->batch == 0) return DECODE_ATTN_OK;
-  SplitLaunch L;
+  SplitLaunch L{};
   const int box_t = std::min(p->page_size, kTile);
   auto encode = plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
                                                          : encode_pool_map;
@@ -458,6 +484,12 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.split = plan.split;
   a.T = num_queries(p);
   a.head_fastest = plan.head_fastest;
+  // Test hook (tensor-core kernel): DECODE_ATTN_TEST_STALL_TX=n makes the
+  // first stage's barrier of every CTA expect n bytes more than the stage
+  // brings, so its wait runs out (about 2 s) and the kernel must report
+  // DECODE_ATTN_DEV_TIMEOUT, write zeros and leave the context usable.  Read
+  // on every call, so a test can set and clear it; unset in normal use.
+  a.stall_tx = env_positive_now("DECODE_ATTN_TEST_STALL_TX");
   a.scale_log2 = p->scale * kLog2e;
   L.grid = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
   L.group_pad = plan.group_pad;

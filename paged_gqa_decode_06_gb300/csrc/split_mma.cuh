@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
         }
         if (abort_s) break;
         const uint32_t fb = smem_u32(&full_bar[st]);
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        // (stall_tx, a test's hook, is 0: the barrier expects the stage's bytes)
+        mbar_arrive_expect_tx(fb, C::kStageBytes + (i == 0 ? a.stall_tx : 0));
         const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
         const uint32_t vdst = kdst + C::kTileBytes;
         for (int pc = 0; pc < pieces_per_tile; ++pc) {

@@ -47,6 +47,7 @@ struct SplitArgs {
   int32_t window, chunk, max_shards, split;
   int32_t T;                  // query positions per sequence (1 for the CUDA-core variant)
   int32_t head_fastest;       // grid (Hkv, S, B) when set, else (S, Hkv, B)
+  int32_t stall_tx;           // 0; a test sets extra bytes on the first stage's barrier
   float scale_log2;           // scale * log2(e)
 };
 

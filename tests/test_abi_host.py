@@ -333,3 +333,29 @@ def test_long_shards_keep_the_deep_ring(pkg):
                      num_pages=8192, max_seq_len=131072)):
         plan = pkg.decode_attn_make_plan(p, 152)
         assert plan.ring_stages == 3 and plan.ctas_per_sm == 2
+
+
+def test_environment_sets_the_planner_defaults():
+    """DECODE_ATTN_SPLIT_MIN / DECODE_ATTN_FORCE_CHUNK are read once per
+    process; a fresh process sees them (the mlx-runner page's
+    MLXR_ATTN_SPLIT_MIN plays this role there)."""
+    import os
+    import subprocess
+    import sys
+    code = ("import paged_gqa_decode_06_gb300 as p; p.load_library(); "
+            "P = p.DecodeAttnParams(batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, "
+            "page_size=16, max_pages_per_seq=192, num_pages=256, max_seq_len=400, scale=0.1, "
+            "window=0, variant=0, split_min=0, force_chunk=0, num_queries=1, dtype=0, "
+            "schedule=0); pl = p.decode_attn_make_plan(P, 152); print(pl.split, pl.chunk_tokens)")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+    def plan_with(env):
+        e = dict(os.environ, **env)
+        r = subprocess.run([sys.executable, "-c", code], cwd=root, env=e, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr
+        return tuple(int(x) for x in r.stdout.split())
+
+    assert plan_with({})[0] == 1                               # 400 > 256: split
+    assert plan_with({"DECODE_ATTN_SPLIT_MIN": "512"})[0] == 0  # threshold moved
+    assert plan_with({"DECODE_ATTN_FORCE_CHUNK": "64"}) == (1, 64)

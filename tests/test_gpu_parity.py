@@ -472,3 +472,30 @@ def test_shallow_ring_parity(pkg, D, Hq, Hkv, dt, window):
     again, _ = run(pkg, w, window=window, max_seq_len=512)
     assert torch.equal(out, again)
     assert torch.all(out[7] == 0)
+
+
+# --------------------------------------------- bounded waits (failure path)
+
+def test_stalled_pipeline_reports_timeout_and_recovers(pkg):
+    """Every CTA's first-stage barrier is made to expect 64 bytes more than
+    its copies bring (the library's DECODE_ATTN_TEST_STALL_TX hook), so the
+    consumers' bounded wait runs out: the call must end by itself with
+    DECODE_ATTN_DEV_TIMEOUT and zero rows, and the next call on the same
+    context must be correct again."""
+    import os
+    w = workloads.make("llama", device=DEV)
+    ws = torch.zeros(pkg.decode_attn_workspace_size(
+        pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len()), 0),
+        dtype=torch.uint8, device=DEV)
+    os.environ["DECODE_ATTN_TEST_STALL_TX"] = "64"
+    try:
+        out, err = run(pkg, w, workspace=ws)
+    finally:
+        del os.environ["DECODE_ATTN_TEST_STALL_TX"]
+    assert err & pkg.DEV_TIMEOUT
+    assert torch.all(out == 0)
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    pkg.decode_attn_workspace_clear(params, ws)
+    out, err = run(pkg, w, workspace=ws)
+    assert err == 0
+    assert_parity(out, oracle_of(w))
