@@ -65,6 +65,9 @@ extern "C" {
 #define DECODE_ATTN_DEV_BAD_PAGE 2      /* page id outside [0, num_pages) in an attended range */
 #define DECODE_ATTN_DEV_OVER_HINT 4     /* seq_len beyond the max_seq_len the grid was planned for */
 #define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed */
+#define DECODE_ATTN_DEV_CHECK 32        /* checked build only (libpaged_gqa_decode_checked.so):
+                                           an index fell outside its buffer; that access was
+                                           skipped (or pointed at the zero-fill coordinate) */
 #define DECODE_ATTN_DEV_WORKSPACE 16    /* a group's shard ticket was not zero on entry:
                                            the group's rows may be stale; clear and retry */
 

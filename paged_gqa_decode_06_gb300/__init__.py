@@ -24,7 +24,7 @@ __all__ = [
     "make_params", "decode_attn", "decode_attn_split", "decode_attn_combine",
     "decode_attn_host", "decode_attn_workspace_size", "decode_attn_make_plan",
     "decode_attn_strerror", "VARIANT_AUTO", "VARIANT_SIMT", "VARIANT_MMA",
-    "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT",
+    "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT", "DEV_CHECK",
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
     "decode_kv_append", "decode_attn_append", "DTYPE_FP16", "DTYPE_BF16",
     "SCHEDULE_AUTO", "SCHEDULE_GRID", "SCHEDULE_PERSISTENT",
@@ -34,11 +34,16 @@ VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
 SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_PERSISTENT = 0, 1, 2
 DTYPE_FP16, DTYPE_BF16 = 0, 1
 DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
+DEV_CHECK = 32  # the checked build only: an index outside its buffer
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def library_path() -> str:
+    """The library this process loads: the checked build (bounds-checked
+    kernels) when DECODE_ATTN_CHECKED=1, else the release build."""
+    if os.environ.get("DECODE_ATTN_CHECKED") == "1":
+        return os.path.join(_HERE, "_build_checked", "libpaged_gqa_decode_checked.so")
     return os.path.join(_HERE, "_build", "libpaged_gqa_decode.so")
 
 

@@ -484,6 +484,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.split = plan.split;
   a.T = num_queries(p);
   a.head_fastest = plan.head_fastest;
+  a.batch = p->batch;
   // Test hook (tensor-core kernel): DECODE_ATTN_TEST_STALL_TX=n makes the
   // first stage's barrier of every CTA expect n bytes more than the stage
   // brings, so its wait runs out (about 2 s) and the kernel must report
@@ -513,11 +514,13 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
 }
 
 int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
-                const int32_t* seq_lens, void* out, const Workspace& ws, cudaStream_t stream) {
+                const int32_t* seq_lens, void* out, const Workspace& ws, int32_t* err_flag,
+                cudaStream_t stream) {
   if (!plan.split || p->batch == 0) return DECODE_ATTN_OK;
   if (plan.persistent) return DECODE_ATTN_OK;  // its merges ran inside the split launch
-  CombineArgs a;
+  CombineArgs a{};
   a.seq_lens = seq_lens;
+  a.err = err_flag;
   a.ws_acc = ws.acc;
   a.ws_ml = ws.ml;
   a.out = out;
@@ -571,7 +574,6 @@ extern "C" int decode_attn_split(const decode_attn_params* p, const void* q, con
 extern "C" int decode_attn_combine(const decode_attn_params* p, const int32_t* seq_lens,
                                    void* out, void* workspace, size_t workspace_bytes,
                                    int32_t* err_flag, void* stream) {
-  (void)err_flag;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   decode_attn_plan plan;
   int st = plan_for_stream(p, s, &plan);
@@ -580,7 +582,7 @@ extern "C" int decode_attn_combine(const decode_attn_params* p, const int32_t* s
   if (!aligned16(out)) return DECODE_ATTN_ERR_ALIGN;
   Workspace ws;
   if ((st = workspace_views(p, plan, workspace, workspace_bytes, &ws))) return st;
-  return run_combine(p, plan, seq_lens, out, ws, s);
+  return run_combine(p, plan, seq_lens, out, ws, err_flag, s);
 }
 
 extern "C" int decode_attn(const decode_attn_params* p, const void* q, const void* k_pages,

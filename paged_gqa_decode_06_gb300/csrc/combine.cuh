@@ -24,8 +24,15 @@ struct CombineArgs {
   const float* ws_acc;   // [B*T*Hq*S_max][D]
   const float2* ws_ml;   // [B*T*Hq*S_max]
   void* out;             // [B][T][Hq][D] 16-bit elements
+  int32_t* err;          // nullable; the checked build's bounds errors
   int32_t B, Hq, G, T, capacity, window, chunk, max_shards;
 };
+
+// Bounds of the partial slots (the checked build; no bound for the
+// persistent schedule's own slots, max_shards = 0).
+__device__ __forceinline__ size_t slot_bound(const CombineArgs& a) {
+  return a.max_shards > 0 ? (size_t)a.B * a.T * a.Hq * a.max_shards : ~size_t(0);
+}
 
 // Output row of the group's r-th query row (r = t * G + g): query t of
 // sequence b, query head h * G + g.
@@ -70,6 +77,11 @@ __device__ __forceinline__ void merge_batch(const CombineArgs& a, int g, int qua
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     const size_t slot = slot_of(g, s + u);
+    if (!PGD_IN(slot, slot_bound(a), a.err)) {
+      x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = make_float2(-INFINITY, 0.f);
+      continue;
+    }
     x[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad);
     v[u] = staged ? ml_s[g * cap + s + u] : __ldcg(a.ws_ml + slot);
   }
@@ -115,14 +127,19 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
     if (cap > 0)
       for (int e = tid; e < G * n; e += nthreads) {
         const int g = e / n, j = e % n;
-        ml_s[g * cap + j] = __ldcg(a.ws_ml + slot_of(g, s0 + j));
+        const size_t slot = slot_of(g, s0 + j);
+        ml_s[g * cap + j] = PGD_IN(slot, slot_bound(a), a.err) ? __ldcg(a.ws_ml + slot)
+                                                                : make_float2(-INFINITY, 0.f);
       }
     sync();
     if (tid < G) {
       float M = max_s[tid];
       int z = zero_s[tid];
       for (int j = 0; j < n; ++j) {
-        const float2 v = cap > 0 ? ml_s[tid * cap + j] : __ldcg(a.ws_ml + slot_of(tid, s0 + j));
+        const size_t slot = slot_of(tid, s0 + j);
+        const float2 v = cap > 0 ? ml_s[tid * cap + j]
+                         : PGD_IN(slot, slot_bound(a), a.err) ? __ldcg(a.ws_ml + slot)
+                                                              : make_float2(-INFINITY, 0.f);
         z |= v.y < 0.f ? 1 : 0;  // a shard saw a bad page or gave up waiting
         M = fmaxf(M, v.x);
       }
@@ -152,10 +169,12 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
       const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
       const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
       const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
-      uint32_t* dst =
-          reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * quad);
-      dst[0] = lo;
-      dst[1] = hi;
+      if (PGD_IN(row, (size_t)a.B * a.T * a.Hq, a.err)) {
+        uint32_t* dst =
+            reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * quad);
+        dst[0] = lo;
+        dst[1] = hi;
+      }
     }
     return;
   }
@@ -190,6 +209,11 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const size_t slot = slot_of(gg[k], s + u);
+          if (!PGD_IN(slot, slot_bound(a), a.err)) {
+            x[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            v[k][u] = make_float2(-INFINITY, 0.f);
+            continue;
+          }
           x[k][u] = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad[k]);
           v[k][u] = staged ? ml_s[gg[k] * cap + s + u] : __ldcg(a.ws_ml + slot);
         }
@@ -209,6 +233,7 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const size_t slot = slot_of(gg[k], s);
+        if (!PGD_IN(slot, slot_bound(a), a.err)) continue;
         const float4 x = __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad[k]);
         const float2 v = staged ? ml_s[gg[k] * cap + s] : __ldcg(a.ws_ml + slot);
         const float c = fast_exp2(v.x - M[k]);
@@ -227,6 +252,7 @@ __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, 
       const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o[k].z, l_sum),
                                             z ? 0.f : __fdiv_rn(o[k].w, l_sum));
       const size_t row = group_row(b, h, gg[k], a.T, a.G, a.Hq);
+      if (!PGD_IN(row, (size_t)a.B * a.T * a.Hq, a.err)) continue;
       uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D +
                                                   4 * quad[k]);
       dst[0] = lo;

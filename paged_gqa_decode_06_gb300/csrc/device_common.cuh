@@ -140,4 +140,20 @@ __device__ __forceinline__ void raise_error(int32_t* err, int32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
+// Bounds checks of the checked build (compiled with PGD_CHECKED; the default
+// build compiles them to `true` and evaluates nothing): an index outside
+// [0, n) raises DECODE_ATTN_DEV_CHECK, and the caller skips the access or
+// redirects it to a harmless one.  Stands in for a memory checker where none
+// can run.
+#ifdef PGD_CHECKED
+__device__ __forceinline__ bool pgd_in_range(uint64_t i, uint64_t n, int32_t* err) {
+  if (i < n) return true;
+  raise_error(err, DECODE_ATTN_DEV_CHECK);
+  return false;
+}
+#define PGD_IN(i, n, err) ::pgd::pgd_in_range((uint64_t)(i), (uint64_t)(n), (err))
+#else
+#define PGD_IN(i, n, err) true
+#endif
+
 }  // namespace pgd

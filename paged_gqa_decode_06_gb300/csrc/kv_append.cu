@@ -22,13 +22,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const KvAppendArgs a) {
     if (rem == 0) raise_error(a.err, DECODE_ATTN_DEV_BAD_LEN);
     return;
   }
-  const int phys = a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
+  const size_t pi = (size_t)b * a.max_pages + pos / a.page_size;
+  if (!PGD_IN(pi, (size_t)a.B * a.max_pages, a.err)) return;
+  const int phys = a.page_table[pi];
   if (phys < 0 || phys >= a.num_pages) {
     if (rem == 0) raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
     return;
   }
   const size_t dst =
       (((size_t)phys * a.page_size + pos % a.page_size) * a.Hkv + h) * a.chunks + c;
+  if (!PGD_IN(dst, (size_t)a.num_pages * a.page_size * a.Hkv * a.chunks, a.err)) return;
   a.k_pages[dst] = a.k_new[idx];
   a.v_pages[dst] = a.v_new[idx];
 }

@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
       const int ptok = shard_lo + i * box_t;
       int coord = oob;
       if (ptok < hi && ptok + box_t > lo) {
-        const int phys = a.page_table[(size_t)b * a.max_pages + (ptok >> a.page_shift)];
+        const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
+        const int phys =
+            PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err) ? a.page_table[pi] : -1;
         if (phys < 0 || phys >= a.num_pages) {
           bad = 1;
         } else {
@@ -285,7 +287,12 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
         const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
         const uint32_t vdst = kdst + C::kTileBytes;
         for (int pc = 0; pc < pieces_per_tile; ++pc) {
-          const int coord = coord_s[i * pieces_per_tile + pc];
+          int coord = coord_s[i * pieces_per_tile + pc];
+          // (checked build) a box must lie inside the pool or start at its
+          // end, where TMA fills zeros
+          const int pool_rows = a.num_pages * a.page_size;
+          if (!PGD_IN(coord == pool_rows ? 0 : (int64_t)coord + box_t - 1, pool_rows, a.err))
+            coord = pool_rows;
 #pragma unroll
           for (int dc = 0; dc < D / 64; ++dc) {
             const uint32_t off = dc * C::kChunkBytes + pc * box_bytes;
@@ -310,8 +317,9 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
 #pragma unroll
   for (int j = 0; j < NT8; ++j) {
     const int rr = 8 * j + gid;
-    const uint16_t* qrow =
-        static_cast<const uint16_t*>(a.q) + group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq) * D;
+    size_t qr = group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq);
+    if (!PGD_IN(qr, (size_t)a.batch * a.T * a.Hq, a.err)) qr = 0;
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + qr * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       if (rr < R) {
@@ -439,6 +447,7 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
       O.w += c * x.w;
     }
     const size_t row = group_row(b, h, g, a.T, G, a.Hq);
+    if (!PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err)) continue;
     if (!a.split) {
       const bool z = dead || ML.y == 0.f;
       const uint32_t lo = (uint32_t)ElemOps<E>::round(z ? 0.f : O.x / ML.y) |
@@ -449,6 +458,7 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
           make_uint2(lo, hi);
     } else {
       const size_t slot = row * a.max_shards + s;
+      if (!PGD_IN(slot, (size_t)a.batch * a.T * a.Hq * a.max_shards, a.err)) continue;
       *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) =
           dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
       if (q == 0) a.ws_ml[slot] = make_float2(ML.x, dead ? -1.f : ML.y);

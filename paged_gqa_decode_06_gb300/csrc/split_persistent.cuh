@@ -471,8 +471,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       named_barrier_sync(1, nthreads);
       if (is_last_s) {
         __threadfence();
-        CombineArgs cm;
+        CombineArgs cm{};
         cm.seq_lens = a.seq_lens;
+        cm.err = a.err;
         cm.ws_acc = a.ws_acc;
         cm.ws_ml = a.ws_ml;
         cm.out = a.out;

@@ -48,6 +48,7 @@ struct SplitArgs {
   int32_t T;                  // query positions per sequence (1 for the CUDA-core variant)
   int32_t head_fastest;       // grid (Hkv, S, B) when set, else (S, Hkv, B)
   int32_t stall_tx;           // 0; a test sets extra bytes on the first stage's barrier
+  int32_t batch;              // B (the checked build's bounds)
   float scale_log2;           // scale * log2(e)
 };
 
@@ -107,7 +108,8 @@ __device__ __forceinline__ void zero_group_rows(const SplitArgs& a, int b, int h
   uint16_t* out = static_cast<uint16_t*>(a.out);  // +0.0 is all zero bits in both formats
   for (int e = threadIdx.x; e < a.T * a.G * D; e += blockDim.x) {
     const int g = e / D, d = e % D;
-    out[group_row(b, h, g, a.T, a.G, a.Hq) * D + d] = 0;
+    const size_t i = group_row(b, h, g, a.T, a.G, a.Hq) * D + d;
+    if (PGD_IN(i, (size_t)a.batch * a.T * a.Hq * D, a.err)) out[i] = 0;
   }
 }
 
@@ -121,10 +123,15 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
   for (int i = 0; i < a.T; ++i) {
     const int pos = r.end - a.T + i;  // position of the i-th new token
     if (pos < shard_lo || pos >= shard_lo + a.chunk || pos < 0) continue;
-    const int phys = a.page_table[(size_t)b * a.max_pages + (pos >> a.page_shift)];
+    const size_t pi = (size_t)b * a.max_pages + (pos >> a.page_shift);
+    if (!PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err)) continue;
+    const int phys = a.page_table[pi];
     const size_t off =
         (((size_t)phys * a.page_size + (pos & (a.page_size - 1))) * a.Hkv + h) * D;
     const size_t src = (((size_t)b * a.T + i) * a.Hkv + h) * D;
+    if (!PGD_IN(off + D - 1, (size_t)a.num_pages * a.page_size * a.Hkv * D, a.err) ||
+        !PGD_IN(src + D - 1, (size_t)a.batch * a.T * a.Hkv * D, a.err))
+      continue;
     const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.k_new) + src);
     const uint4* vs = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.v_new) + src);
     uint4* kd = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.k_pages_w) + off);
@@ -149,6 +156,7 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   __threadfence();  // this thread's partial writes, visible GPU-wide
   named_barrier_sync(1, nthreads);
   int32_t* ticket = a.counters + (size_t)b * a.Hkv + h;
+  if (!PGD_IN((size_t)b * a.Hkv + h, (size_t)a.batch * a.Hkv, a.err)) return;
   if (threadIdx.x == 0) {
     const int old = atomicAdd(ticket, 1);
     if (old < 0 || old >= r.nshards) raise_error(a.err, DECODE_ATTN_DEV_WORKSPACE);
@@ -157,12 +165,13 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   named_barrier_sync(1, nthreads);
   if (!is_last_s) return;
   __threadfence();
-  CombineArgs c;
+  CombineArgs c{};
   c.seq_lens = a.seq_lens;
   c.ws_acc = a.ws_acc;
   c.ws_ml = a.ws_ml;
   c.out = a.out;
-  c.B = 0;
+  c.err = a.err;
+  c.B = a.batch;
   c.Hq = a.Hq;
   c.G = a.G;
   c.T = a.T;
@@ -241,7 +250,9 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
       const int ptok = shard_lo + i * box_t;
       int coord = oob;
       if (ptok < hi && ptok + box_t > lo) {
-        const int phys = a.page_table[(size_t)b * a.max_pages + (ptok >> a.page_shift)];
+        const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
+        const int phys =
+            PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err) ? a.page_table[pi] : -1;
         if (phys < 0 || phys >= a.num_pages) {
           bad = 1;
         } else {
@@ -290,7 +301,10 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
         const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
         const uint32_t vdst = kdst + C::kTileBytes;
         for (int pc = 0; pc < pieces_per_tile; ++pc) {
-          const int coord = coord_s[i * pieces_per_tile + pc];
+          int coord = coord_s[i * pieces_per_tile + pc];
+          const int pool_rows = a.num_pages * a.page_size;  // (checked build) see split_mma
+          if (!PGD_IN(coord == pool_rows ? 0 : (int64_t)coord + box_t - 1, pool_rows, a.err))
+            coord = pool_rows;
           tma_load_3d(kdst + pc * box_bytes, &tmap_k, 0, h, coord, fb);
           tma_load_3d(vdst + pc * box_bytes, &tmap_v, 0, h, coord, fb);
         }
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   float qf[GP][DPL];
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
-    if (g < G) {
+    if (g < G && PGD_IN((size_t)b * a.Hq + h * G + g, (size_t)a.batch * a.Hq, a.err)) {
       load_f16_row<DPL>(static_cast<const __half*>(a.q) + ((size_t)b * a.Hq + h * G + g) * D +
                             lane * DPL,
                         qf[g]);
@@ -422,10 +436,12 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
       O += c * acc_s[(w * GP + g) * D + d];
     }
     const size_t row = (size_t)b * a.Hq + h * G + g;
+    if (!PGD_IN(row, (size_t)a.batch * a.Hq, a.err)) continue;
     if (!a.split) {
       static_cast<__half*>(a.out)[row * D + d] = __float2half_rn((dead || L == 0.f) ? 0.f : O / L);
     } else {
       const size_t slot = row * a.max_shards + s;
+      if (!PGD_IN(slot, (size_t)a.batch * a.Hq * a.max_shards, a.err)) continue;
       a.ws_acc[slot * D + d] = dead ? 0.f : O;
       if (d == 0) a.ws_ml[slot] = make_float2(M, dead ? -1.f : L);
     }
