@@ -174,10 +174,10 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
   }
 }
 
-template <int D, int NT8, class E, bool SH = false>
-__global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
-    split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+// The split kernel's body, shared by the two kernels below.
+template <int D, int NT8, class E, bool SH>
+__device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
+                                               const CUtensorMap& tmap_v, const SplitArgs& a) {
   using C = MmaCfg<D, SH>;
   constexpr int GP = 8 * NT8;  // padded heads of the group
   constexpr int KS = D / 16;   // k-steps of q.k, m-tiles of p.v
@@ -465,6 +465,26 @@ __global__ void __launch_bounds__(MmaCfg<D, SH>::kThreads, SH ? 3 : 1)
     }
   }
   if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
+}
+
+// The split kernel with the deep ring.  Its launch bounds name no CTA count:
+// the register allocation it gets that way (128 at D = 128 with one n8 tile,
+// 166 with two) leaves two CTAs per SM; naming one CTA per SM instead gave
+// the two-tile kernel 205 registers, one CTA per SM and a 20 % slower T = 2
+// long step.
+template <int D, int NT8, class E>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads)
+    split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+  split_mma_body<D, NT8, E, false>(tmap_k, tmap_v, a);
+}
+
+// The split kernel with the shallow ring: registers capped for 3 CTAs per SM.
+template <int D, int NT8, class E>
+__global__ void __launch_bounds__(MmaCfg<D, true>::kThreads, 3)
+    split_mma_kernel_shallow(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+  split_mma_body<D, NT8, E, true>(tmap_k, tmap_v, a);
 }
 
 }  // namespace pgd
