@@ -76,11 +76,16 @@ extern "C" {
 #define DECODE_ATTN_DTYPE_BF16 1        /* bfloat16 (tensor-core variant) */
 
 /* Work schedules of the split kernel (decode_attn_params.schedule). */
-#define DECODE_ATTN_SCHEDULE_AUTO 0       /* planner picks (the grid schedule) */
-#define DECODE_ATTN_SCHEDULE_GRID 1       /* one CTA per (shard, KV head, sequence) */
+#define DECODE_ATTN_SCHEDULE_AUTO 0       /* planner picks (grid, or cluster where it gains) */
+#define DECODE_ATTN_SCHEDULE_GRID 1       /* one CTA per (shard, KV head, sequence); the
+                                             last CTA of a group merges via the workspace */
 #define DECODE_ATTN_SCHEDULE_PERSISTENT 2 /* one CTA per resident slot, equal tile ranges
                                              of the flattened (sequence, KV head, tile) list;
                                              tensor-core variant, B <= 1024 */
+#define DECODE_ATTN_SCHEDULE_CLUSTER 3    /* grid schedule whose shards of one (KV head,
+                                             sequence) form a thread-block cluster and merge
+                                             through distributed shared memory; one-wave
+                                             split plans of 2..8 shards, tensor-core variant */
 
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
@@ -129,6 +134,9 @@ typedef struct decode_attn_plan {
   int32_t ring_stages;       /* 64-token K/V stages in flight per CTA: 3 (6 at D=64);
                                 2 (4 at D=64) for grids of several waves of short
                                 shards, which fit 3 CTAs per SM (tensor-core variant) */
+  int32_t cluster;           /* CTAs per thread-block cluster (the shards of one
+                                (KV head, sequence), merged through distributed shared
+                                memory), or 0 (merged through the workspace) */
   size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;

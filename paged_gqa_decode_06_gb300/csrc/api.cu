@@ -21,6 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMinChunk = 128;        // shortest shard the planner picks, tokens
 constexpr int kLargeChunkCap = 2048;  // longest shard for large work, unless span / 16
 constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 // Cost model of a one-wave split plan, calibrated on GB300 chunk sweeps (one,
 // two and four sequences of 16 Ki..128 Ki tokens, the Llama-3.1-8B shape, the
 // windowed long case):
@@ -93,7 +94,7 @@ int check_params(const decode_attn_params* p) {
   if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
   if (p->dtype != DECODE_ATTN_DTYPE_FP16 && p->dtype != DECODE_ATTN_DTYPE_BF16)
     return DECODE_ATTN_ERR_SHAPE;
-  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_PERSISTENT) return DECODE_ATTN_ERR_SHAPE;
+  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_CLUSTER) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -331,6 +332,27 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   plan->grid_y = head_fastest ? (int32_t)max_shards : p->num_kv_heads;
   plan->grid_z = p->batch;
   plan->ctas_per_sm = cps;
+  // Cluster merge: the shards of a (KV head, sequence) as one thread-block
+  // cluster (grid x = shards), merged through distributed shared memory
+  // instead of the workspace and a ticket, for one-wave tensor-core split
+  // plans of 2..8 shards (a portable cluster).  The planner takes it when the
+  // grid fills at least 4/5 of the CTA slots or the step is small: a cluster's
+  // CTAs are packed onto neighbouring SMs of one GPC, so a sparse grid of
+  // clusters leaves SMs idle.  GB300, against the workspace merge on the same
+  // plans: long case 305.4 -> 303.3 us, window 4096 23.2 -> 22.5 us, four
+  // 32768-token sequences 85.2 -> 84.2 us, the D = 64 sweep shape 14.9 ->
+  // 14.4 us; two 65536-token sequences at 8 shards (128 CTAs) 93.2 -> 104.5.
+  const bool cluster_ok = variant == DECODE_ATTN_VARIANT_MMA && plan->split && !head_fastest &&
+                          !shallow && max_shards >= 2 && max_shards <= kMaxCluster;
+  const int64_t step_bytes =
+      (int64_t)p->batch * p->num_kv_heads * span * 4 * p->head_dim;
+  if (p->schedule == DECODE_ATTN_SCHEDULE_CLUSTER) {
+    if (!cluster_ok) return DECODE_ATTN_ERR_VARIANT;
+    plan->cluster = (int32_t)max_shards;
+  } else if (p->schedule == DECODE_ATTN_SCHEDULE_AUTO && cluster_ok &&
+             (ctas * 5 >= slots_all * 4 || step_bytes <= (int64_t(32) << 20))) {
+    plan->cluster = (int32_t)max_shards;
+  }
   if (plan->split) {
     // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
     const size_t rows = (size_t)p->batch * T * p->num_q_heads * (size_t)max_shards;
@@ -497,6 +519,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.variant = plan.variant;
   L.dtype = p->dtype;
   L.persistent = plan.persistent;
+  L.cluster = plan.cluster;
   L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && !plan.persistent &&
                p->head_dim <= 128 && plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
                   ? 1

@@ -174,8 +174,29 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
   }
 }
 
-// The split kernel's body, shared by the two kernels below.
-template <int D, int NT8, class E, bool SH>
+// Where a CTA of a cluster plan keeps its shard's partial for the cluster's
+// merge: after the warps' states in the (by then idle) ring, out [GP][D]
+// fp32, then (m, l) [GP] float2 (l = -1: a dead shard).
+template <int D, int NT8>
+struct ClusterPartial {
+  static constexpr int kRowStride = D + 4;
+  static constexpr int kOutOffset = ((MmaCfg<D>::kWarps * 8 * NT8 * kRowStride * 4) + 15) & ~15;
+  static constexpr int kMlOffset = kOutOffset + 8 * NT8 * D * 4;
+  static constexpr int kEnd = kMlOffset + 8 * NT8 * 8;
+  static_assert(kEnd <= MmaCfg<D>::kRingBytes, "the partial fits in the ring");
+};
+
+__device__ __forceinline__ uint8_t* ring_base() {
+  extern __shared__ uint8_t smem_raw[];
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                    ~uintptr_t(1023));
+}
+
+// The split kernel's body, shared by the kernels below.  CL: a cluster plan
+// (one cluster per (KV head, sequence), one CTA per shard): the CTA leaves
+// its partial in its shared memory (and in the workspace, for
+// decode_attn_combine) and the kernel's cluster merge follows.
+template <int D, int NT8, class E, bool SH, bool CL = false>
 __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
                                                const CUtensorMap& tmap_v, const SplitArgs& a) {
   using C = MmaCfg<D, SH>;
@@ -211,9 +232,21 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
                                a.max_shards, a.T);
   if (r.status != 0 || s >= r.nshards) {
-    if (s == 0) {
-      if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
-      zero_group_rows<D, GP>(a, b, h);
+    if constexpr (CL) {
+      // an empty partial (no position of any row); the cluster merge zeroes
+      // rows that no shard holds
+      if (s == 0 && r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
+      using P = ClusterPartial<D, NT8>;
+      uint8_t* base = ring_base();
+      float* po = reinterpret_cast<float*>(base + P::kOutOffset);
+      float2* pml = reinterpret_cast<float2*>(base + P::kMlOffset);
+      for (int e = threadIdx.x; e < GP * D; e += blockDim.x) po[e] = 0.f;
+      for (int g = threadIdx.x; g < GP; g += blockDim.x) pml[g] = make_float2(-INFINITY, 0.f);
+    } else {
+      if (s == 0) {
+        if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
+        zero_group_rows<D, GP>(a, b, h);
+      }
     }
     return;
   }
@@ -457,14 +490,115 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + row * D + 4 * q) =
           make_uint2(lo, hi);
     } else {
+      const float4 Ow = dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
+      const float2 MLw = make_float2(ML.x, dead ? -1.f : ML.y);
+      if constexpr (CL) {
+        using P = ClusterPartial<D, NT8>;
+        *reinterpret_cast<float4*>(ring + P::kOutOffset + (g * D + 4 * q) * 4) = Ow;
+        if (q == 0) reinterpret_cast<float2*>(ring + P::kMlOffset)[g] = MLw;
+      }
       const size_t slot = row * a.max_shards + s;
       if (!PGD_IN(slot, (size_t)a.batch * a.T * a.Hq * a.max_shards, a.err)) continue;
-      *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) =
-          dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
-      if (q == 0) a.ws_ml[slot] = make_float2(ML.x, dead ? -1.f : ML.y);
+      *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) = Ow;
+      if (q == 0) a.ws_ml[slot] = MLw;
     }
   }
-  if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
+  if constexpr (!CL) {
+    if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
+  }
+}
+
+// %cluster_ctarank / %cluster_nctarank, the cluster-wide barrier (every
+// thread of every CTA of the cluster; the release / acquire pair orders the
+// partials written before it with the reads after it) and loads from another
+// CTA's shared memory.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// The cluster merge: every thread of the cluster's CTAs arrives here once the
+// body has returned (on any path); after the barrier each CTA merges its
+// slice of the group's (row, 4 dims) items from all the cluster's partials
+// in ascending shard (= cluster rank) order with merge_group's arithmetic
+// (max, then c_s = 2^(m_s - M) with fused multiply-adds), so the bits equal
+// the workspace merge's; a second barrier keeps every CTA's shared memory
+// alive until the last read.
+template <int D, int NT8, class E>
+__device__ __forceinline__ void cluster_merge(const SplitArgs& a) {
+  using P = ClusterPartial<D, NT8>;
+  constexpr int kQuads = D / 4;
+  __syncwarp();
+  cluster_sync_all();
+  const uint32_t S = cluster_size(), rank = cluster_rank();
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int R = a.T * a.G, total = R * kQuads;
+  const int per = (total + (int)S - 1) / (int)S;
+  const int e_end = min(total, ((int)rank + 1) * per);
+  uint8_t* base = ring_base();
+  for (int e = (int)rank * per + (int)threadIdx.x; e < e_end; e += (int)blockDim.x) {
+    const int g = e / kQuads, q = e % kQuads;
+    const float2* ml_local = reinterpret_cast<const float2*>(base + P::kMlOffset) + g;
+    const float* o_local = reinterpret_cast<const float*>(base + P::kOutOffset) + g * D + 4 * q;
+    float M = -INFINITY;
+    bool z = false;
+    for (uint32_t j = 0; j < S; ++j) {
+      const float2 v = ld_dsmem_f2(dsmem_addr(ml_local, j));
+      z |= v.y < 0.f;  // a shard saw a bad page or gave up waiting
+      M = fmaxf(M, v.x);
+    }
+    z |= M == -INFINITY;  // no shard holds a position of this row
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (uint32_t j = 0; !z && j < S; ++j) {
+      const float2 v = ld_dsmem_f2(dsmem_addr(ml_local, j));
+      const float4 x = ld_dsmem_f4(dsmem_addr(o_local, j));
+      const float c = fast_exp2(v.x - M);
+      L = __fmaf_rn(c, v.y, L);
+      o.x = __fmaf_rn(c, x.x, o.x);
+      o.y = __fmaf_rn(c, x.y, o.y);
+      o.z = __fmaf_rn(c, x.z, o.z);
+      o.w = __fmaf_rn(c, x.w, o.w);
+    }
+    z |= L == 0.f;
+    const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
+    const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
+    const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
+    if (PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err)) {
+      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * q);
+      dst[0] = lo;
+      dst[1] = hi;
+    }
+  }
+  cluster_sync_all();
 }
 
 // The split kernel with the deep ring.  Its launch bounds name no CTA count:
@@ -477,6 +611,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
   split_mma_body<D, NT8, E, false>(tmap_k, tmap_v, a);
+}
+
+// The split kernel of cluster plans (grid (S, Hkv, B), clusters of the S
+// shards of one (KV head, sequence)): the merge goes through distributed
+// shared memory instead of the workspace and a ticket.
+template <int D, int NT8, class E>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads)
+    split_mma_kernel_cluster(const __grid_constant__ CUtensorMap tmap_k,
+                             const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+  split_mma_body<D, NT8, E, false, true>(tmap_k, tmap_v, a);
+  cluster_merge<D, NT8, E>(a);
 }
 
 // The split kernel with the shallow ring: registers capped for 3 CTAs per SM.

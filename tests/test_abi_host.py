@@ -359,3 +359,29 @@ def test_environment_sets_the_planner_defaults():
     assert plan_with({})[0] == 1                               # 400 > 256: split
     assert plan_with({"DECODE_ATTN_SPLIT_MIN": "512"})[0] == 0  # threshold moved
     assert plan_with({"DECODE_ATTN_FORCE_CHUNK": "64"}) == (1, 64)
+
+
+def test_cluster_plans(pkg):
+    """One-wave tensor-core split plans of 2..8 shards merge inside a
+    thread-block cluster when the grid fills most CTA slots or the step is
+    small; the grid schedule and longer shard lists merge through the
+    workspace; asking for a cluster where none applies is an error."""
+    long4 = dict(batch=4, num_q_heads=64, num_kv_heads=8, page_size=64, max_pages_per_seq=2048,
+                 num_pages=8192, max_seq_len=131072)
+    plan = pkg.decode_attn_make_plan(params(pkg, **long4), 152)
+    assert plan.cluster == plan.max_shards == 8 and plan.head_fastest == 0
+    plan = pkg.decode_attn_make_plan(params(pkg, **long4, window=4096), 152)
+    assert plan.cluster == plan.max_shards
+    plan = pkg.decode_attn_make_plan(params(pkg, **long4, schedule=1), 152)
+    assert plan.cluster == 0
+    plan = pkg.decode_attn_make_plan(params(pkg), 152)   # Llama shape: 16 shards
+    assert plan.max_shards > 8 and plan.cluster == 0
+    with pytest.raises(pkg.DecodeAttnError):
+        pkg.decode_attn_make_plan(params(pkg, schedule=3), 152)
+    plan = pkg.decode_attn_make_plan(params(pkg, schedule=3, force_chunk=384), 152)
+    assert plan.cluster == plan.max_shards == 8
+    # a sparse grid of clusters (128 CTAs, 537 MB) keeps the workspace merge
+    plan = pkg.decode_attn_make_plan(
+        params(pkg, batch=2, num_q_heads=64, page_size=64, max_pages_per_seq=1024,
+               num_pages=2048, max_seq_len=65536, force_chunk=8192), 152)
+    assert plan.max_shards == 8 and plan.cluster == 0
