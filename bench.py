@@ -25,6 +25,7 @@ import hashlib
 import glob
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -232,6 +233,33 @@ def recorded_traffic(workload: str):
 
 # ------------------------------------------------------------ CPU oracle
 
+def cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo (x86 'model name'; on Arm the
+    implementer/part codes when no name is given)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model Name", "Hardware"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", info, re.M)
+        if m:
+            return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, re.M)
+    if imp and part:
+        return f"{platform.machine()} implementer {imp.group(1)} part {part.group(1)}"
+    return platform.machine()
+
+
+def percentiles_us(ms_list):
+    """p10 / median / p90 of per-step times given in ms, in us."""
+    import numpy as np
+    a = np.asarray(ms_list, dtype=np.float64) * 1e3
+    return {"p10": float(np.percentile(a, 10)), "p50": float(np.percentile(a, 50)),
+            "p90": float(np.percentile(a, 90))}
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -418,7 +446,7 @@ def gpu_arm(args):
     barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    total_ms, _ = timed_loop(run_step)
+    total_ms, step_ms = timed_loop(run_step)
     t_wall1 = time.time()
     barrier()
     # split kernel alone, each launch bracketed by events on its stream
@@ -479,7 +507,13 @@ def gpu_arm(args):
         smp = OracleSample(w.to("cpu"), cores).calibrate(args.cpu_budget)
         nbytes, secs = smp.run()
         cpu = {"value": nbytes / secs / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
-               "sample": smp.describe(nbytes), "seconds": round(secs, 2)}
+               "sample": smp.describe(nbytes), "seconds": round(secs, 2), "cpu": cpu_model()}
+        if w.kv_bytes() < (1 << 30) and cores > 1:
+            # the smaller workloads: the same sample on one thread as well
+            one = OracleSample(w.to("cpu"), 1).calibrate(min(5.0, args.cpu_budget))
+            nb1, secs1 = one.run()
+            cpu["one_thread"] = {"value": nb1 / secs1 / 1e12, "unit": "TB/s",
+                                 "sample": one.describe(nb1), "seconds": round(secs1, 2)}
 
     clocks = sampler.summary(t_wall0, t_wall1)
     if rank == 0:
@@ -497,12 +531,15 @@ def gpu_arm(args):
                               f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"),
                        "plan": plan.as_dict(), "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "split_simt_kernel" if plan.variant == 1
+                         else "split_allheads_kernel" if plan.all_heads
                          else "split_mma_kernel",
                          "achieved": split_achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": split_achieved_gbs / peak_gbs, "peak_source": peak_src,
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": kv_bytes,
-                         "launch_us": split_avg_ms * 1e3},
+                         "launch_us": split_avg_ms * 1e3,
+                         "launch_us_percentiles": percentiles_us(split_ms)},
+            "step_us_percentiles": percentiles_us(step_ms) if step_ms else None,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K,
             "launch_mode": "eager" if args.eager else "cuda graph replay",
@@ -619,7 +656,7 @@ def reference_arm(args):
         "impl": "reference",
         "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {desc}"},
+                         "sample": f"per step: {desc}", "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

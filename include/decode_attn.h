@@ -86,6 +86,14 @@ extern "C" {
                                              sequence) form a thread-block cluster and merge
                                              through distributed shared memory; one-wave
                                              split plans of 2..8 shards, tensor-core variant */
+#define DECODE_ATTN_SCHEDULE_ALL_HEADS 4  /* one persistent CTA per SM takes (sequence, shard)
+                                             items from a counter and streams 16-position
+                                             slices of all 8 KV heads per stage (whole page
+                                             rows), one consumer warp per KV head; the warp
+                                             that completes a (sequence, KV head) merges it.
+                                             Tensor-core variant, D 64 or 128, Hkv = 8,
+                                             G <= 8, T = 1, page_size >= 16; used only
+                                             when asked for */
 
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
@@ -137,7 +145,9 @@ typedef struct decode_attn_plan {
   int32_t cluster;           /* CTAs per thread-block cluster (the shards of one
                                 (KV head, sequence), merged through distributed shared
                                 memory), or 0 (merged through the workspace) */
-  size_t workspace_bytes;    /* tickets max(64 KiB, B*Hkv*4) + partials B*Hq*S_max*(D+2)*4,
+  int32_t all_heads;         /* 1: the all-heads schedule (grid_x = SMs, one CTA each;
+                                tile_tokens = 16 positions per stage of all KV heads) */
+  size_t workspace_bytes;    /* tickets max(64 KiB, (B*Hkv+64)*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;
 

@@ -28,10 +28,12 @@ __all__ = [
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
     "decode_kv_append", "decode_attn_append", "DTYPE_FP16", "DTYPE_BF16",
     "SCHEDULE_AUTO", "SCHEDULE_GRID", "SCHEDULE_PERSISTENT", "SCHEDULE_CLUSTER",
+    "SCHEDULE_ALL_HEADS",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
 SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_PERSISTENT, SCHEDULE_CLUSTER = 0, 1, 2, 3
+SCHEDULE_ALL_HEADS = 4
 DTYPE_FP16, DTYPE_BF16 = 0, 1
 DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
 DEV_CHECK = 32  # the checked build only: an index outside its buffer
@@ -61,7 +63,7 @@ class DecodeAttnPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "split", "variant", "group_pad", "tile_tokens", "chunk_tokens", "max_shards",
         "grid_x", "grid_y", "grid_z", "ctas_per_sm", "persistent", "head_fastest",
-        "ring_stages", "cluster")] + [
+        "ring_stages", "cluster", "all_heads")] + [
         ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):

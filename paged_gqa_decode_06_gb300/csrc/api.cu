@@ -22,6 +22,9 @@ constexpr int kMinChunk = 128;        // shortest shard the planner picks, token
 constexpr int kLargeChunkCap = 2048;  // longest shard for large work, unless span / 16
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kMaxCluster = 8;  // portable thread-block cluster size
+constexpr int kAllHeadsKv = 8;            // KV heads of the all-heads kernel (its consumer warps)
+constexpr int64_t kAllHeadsMinChunk = 256;
+constexpr int64_t kAllHeadsMaxChunk = 1024;  // its per-item page-row table
 // Cost model of a one-wave split plan, calibrated on GB300 chunk sweeps (one,
 // two and four sequences of 16 Ki..128 Ki tokens, the Llama-3.1-8B shape, the
 // windowed long case):
@@ -94,7 +97,7 @@ int check_params(const decode_attn_params* p) {
   if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
   if (p->dtype != DECODE_ATTN_DTYPE_FP16 && p->dtype != DECODE_ATTN_DTYPE_BF16)
     return DECODE_ATTN_ERR_SHAPE;
-  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_CLUSTER) return DECODE_ATTN_ERR_SHAPE;
+  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_ALL_HEADS) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -103,8 +106,9 @@ int check_params(const decode_attn_params* p) {
 // has more groups: a zero-filled workspace therefore stays valid across calls
 // with different shapes, since every completed call leaves its tickets zero.
 constexpr size_t kTicketRegion = 64 * 1024;
+// Group tickets [B*Hkv], then the all-heads schedule's work counters.
 size_t ticket_region_bytes(const decode_attn_params* p) {
-  const size_t need = ((size_t)p->batch * p->num_kv_heads * 4 + 255) / 256 * 256;
+  const size_t need = (((size_t)p->batch * p->num_kv_heads + 64) * 4 + 255) / 256 * 256;
   return need > kTicketRegion ? need : kTicketRegion;
 }
 
@@ -353,9 +357,52 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
              (ctas * 5 >= slots_all * 4 || step_bytes <= (int64_t(32) << 20))) {
     plan->cluster = (int32_t)max_shards;
   }
+  // All-heads schedule, on request: one persistent CTA per SM streams
+  // 16-position slices of all 8 KV heads per stage (whole page rows) instead
+  // of one head's rows per CTA.  A streaming probe without arithmetic read
+  // the batched workload's page-16 pool at 7.13 TB/s that way (6.25 with
+  // per-head 2 KB boxes), but the kernel itself measured behind the grid
+  // schedule on GB300 (batched 208 vs 193 us, a thousand short sequences 186
+  // vs 180 us): one CTA's eight consumer warps sustain about 49 GB/s, so the
+  // tail and the item boundaries cost more than the better reads gain.
+  const bool ah_ok = variant == DECODE_ATTN_VARIANT_MMA &&
+                     (p->head_dim == 64 || p->head_dim == 128) &&
+                     p->num_kv_heads == kAllHeadsKv && T == 1 && group_pad == 8 &&
+                     p->page_size >= 16 && p->batch >= 1;
+  int64_t ah_chunk = 0;
+  if (ah_ok) {
+    ah_chunk = force_chunk > 0
+                   ? round_up(force_chunk, kTile)
+                   : std::min<int64_t>(kAllHeadsMaxChunk,
+                                       std::max<int64_t>(kAllHeadsMinChunk,
+                                                         round_up(ceil_div(span, 16), kTile)));
+  }
+  bool all_heads = false;
+  if (p->schedule == DECODE_ATTN_SCHEDULE_ALL_HEADS) {
+    if (!ah_ok || ah_chunk > kAllHeadsMaxChunk) return DECODE_ATTN_ERR_VARIANT;
+    all_heads = true;
+  }
+  if (all_heads) {
+    const int64_t shards = ceil_div(span, ah_chunk);
+    if (shards > 65535 || (int64_t)p->batch * shards > (int64_t(1) << 30))
+      return DECODE_ATTN_ERR_SHAPE;
+    plan->split = 1;
+    plan->tile_tokens = 16;
+    plan->chunk_tokens = (int32_t)ah_chunk;
+    plan->max_shards = (int32_t)shards;
+    plan->grid_x = num_sms;
+    plan->grid_y = 1;
+    plan->grid_z = 1;
+    plan->ctas_per_sm = 1;
+    plan->persistent = 0;
+    plan->head_fastest = 0;
+    plan->cluster = 0;
+    plan->all_heads = 1;
+    plan->ring_stages = p->head_dim == 64 ? 6 : 3;
+  }
   if (plan->split) {
     // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
-    const size_t rows = (size_t)p->batch * T * p->num_q_heads * (size_t)max_shards;
+    const size_t rows = (size_t)p->batch * T * p->num_q_heads * (size_t)plan->max_shards;
     plan->workspace_bytes = ticket_region_bytes(p) + round_up(rows * sizeof(float2), 256) +
                             round_up(rows * p->head_dim * 4, 256);
   }
@@ -398,18 +445,46 @@ int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params
   return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
 }
 
-// 4-D view (64 dims, D/64 chunks, kv head, P*PS token rows) with the 128-byte
-// swizzle: one box = box_t rows x 64 dims of one head, written to shared
-// memory as [box_t][64] with 16-byte chunk c of row t at chunk c ^ (t % 8).
+// 4-D view (64 dims, P*PS token rows, kv head, D/64 chunks) with the 128-byte
+// swizzle, written to shared memory as [D/64][box_t][64] per box_t rows
+// (16-byte chunk c of row t at c ^ (t % 8)).  Pieces shorter than 64 rows
+// take one box for all D dims: on GB300 one CTA copying per-chunk boxes of
+// 16 rows (2 KB) was capped near 45 GB/s, and the batched workload (pages
+// of 16) went from 197.2 to 193-195 us with the whole piece in one box.
+// 64-row pieces keep one box per 64-dim chunk (8 KB each), which measured
+// faster there (one 131072-token sequence 89.1 against 90.2 us).
 int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_attn_params* p,
                              int box_t) {
   auto fn = encode_fn();
   if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
   const int D = p->head_dim;
-  cuuint64_t dims[4] = {64, (cuuint64_t)D / 64, (cuuint64_t)p->num_kv_heads,
-                        (cuuint64_t)p->num_pages * p->page_size};
-  cuuint64_t strides[3] = {128, (cuuint64_t)D * 2, (cuuint64_t)p->num_kv_heads * D * 2};
-  cuuint32_t box[4] = {64, 1, 1, (cuuint32_t)box_t};
+  cuuint64_t dims[4] = {64, (cuuint64_t)p->num_pages * p->page_size,
+                        (cuuint64_t)p->num_kv_heads, (cuuint64_t)D / 64};
+  cuuint64_t strides[3] = {(cuuint64_t)p->num_kv_heads * D * 2, (cuuint64_t)D * 2, 128};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_t, 1, box_t < kTile ? (cuuint32_t)D / 64 : 1u};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
+                                    ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, et, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
+}
+
+// 4-D view (64 dims, P*PS token rows, kv head, D/64 chunks) with the 128-byte
+// swizzle, for the all-heads kernel: one box = 16 rows x all Hkv heads x 64
+// dims, written to shared memory as [head][16 rows][64 dims] (row t of head
+// h is 128-byte row 16h + t, its 16-byte chunk c at c ^ (t % 8)).
+int encode_pool_map_heads(CUtensorMap* map, const void* base, const decode_attn_params* p,
+                          int /*box_t*/) {
+  auto fn = encode_fn();
+  if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
+  const int D = p->head_dim;
+  cuuint64_t dims[4] = {64, (cuuint64_t)p->num_pages * p->page_size,
+                        (cuuint64_t)p->num_kv_heads, (cuuint64_t)D / 64};
+  cuuint64_t strides[3] = {(cuuint64_t)p->num_kv_heads * D * 2, (cuuint64_t)D * 2, 128};
+  cuuint32_t box[4] = {64, 16, (cuuint32_t)p->num_kv_heads, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -474,8 +549,9 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   if (p->batch == 0) return DECODE_ATTN_OK;
   SplitLaunch L{};
   const int box_t = std::min(p->page_size, kTile);
-  auto encode = plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
-                                                         : encode_pool_map;
+  auto encode = plan.all_heads ? encode_pool_map_heads
+                : plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
+                                                           : encode_pool_map;
   int st = encode(&L.tmap_k, k_pages, p, box_t);
   if (!st) st = encode(&L.tmap_v, v_pages, p, box_t);
   if (st) return st;
@@ -520,7 +596,8 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.dtype = p->dtype;
   L.persistent = plan.persistent;
   L.cluster = plan.cluster;
-  L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && !plan.persistent &&
+  L.all_heads = plan.all_heads;
+  L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && !plan.persistent && !plan.all_heads &&
                p->head_dim <= 128 && plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
                   ? 1
                   : 0;  // the launcher has the shallow kernels the planner picks from
@@ -529,6 +606,28 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.stream = stream;
   // the shard tickets are zero on entry: the last CTA of each group clears
   // its own, so a workspace cleared once stays clear across calls
+  if (plan.all_heads && k_new != nullptr) {
+    // the all-heads kernel has no fused append: the step's rows go to their
+    // pages first (positions seq_lens[b] - 1), then the attention reads them
+    KvAppendArgs ka;
+    ka.k_new = static_cast<const uint4*>(k_new);
+    ka.v_new = static_cast<const uint4*>(v_new);
+    ka.positions = seq_lens;
+    ka.pos_offset = -1;
+    ka.page_table = page_table;
+    ka.k_pages = static_cast<uint4*>(const_cast<void*>(k_pages));
+    ka.v_pages = static_cast<uint4*>(const_cast<void*>(v_pages));
+    ka.err = err_flag;
+    ka.B = p->batch;
+    ka.Hkv = p->num_kv_heads;
+    ka.chunks = p->head_dim / 8;
+    ka.page_size = p->page_size;
+    ka.max_pages = p->max_pages_per_seq;
+    ka.num_pages = p->num_pages;
+    if ((st = cuda_status(launch_kv_append(ka, stream)))) return st;
+    a.k_new = nullptr;
+    a.v_new = nullptr;
+  }
   switch (p->head_dim) {
     case 64: return cuda_status(launch_split_d64(L));
     case 128: return cuda_status(launch_split_d128(L));
@@ -655,6 +754,7 @@ extern "C" int decode_kv_append(const decode_attn_params* p, const void* k_new, 
   a.k_new = static_cast<const uint4*>(k_new);
   a.v_new = static_cast<const uint4*>(v_new);
   a.positions = positions;
+  a.pos_offset = 0;
   a.page_table = page_table;
   a.k_pages = static_cast<uint4*>(k_pages);
   a.v_pages = static_cast<uint4*>(v_pages);

@@ -16,7 +16,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const KvAppendArgs a) {
   const int b = (int)(idx / per_seq);
   const int rem = (int)(idx % per_seq);
   const int h = rem / a.chunks, c = rem % a.chunks;
-  const int pos = a.positions[b];
+  const int pos = a.positions[b] + a.pos_offset;
   if (pos < 0) return;
   if (pos >= a.max_pages * a.page_size) {
     if (rem == 0) raise_error(a.err, DECODE_ATTN_DEV_BAD_LEN);

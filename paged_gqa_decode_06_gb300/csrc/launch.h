@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "combine.cuh"
+#include "split_allheads.cuh"
 #include "split_mma.cuh"
 #include "split_persistent.cuh"
 #include "split_simt.cuh"
@@ -23,6 +24,7 @@ struct SplitLaunch {
   int persistent;   // launch the persistent kernel (at most grid.x CTAs)
   int shallow;      // tensor-core kernel with the shallow ring (MmaCfg kShallow)
   int cluster;      // > 0: the cluster-merge kernel, clusters of this many CTAs along x
+  int all_heads;    // the all-heads kernel (grid.x CTAs, one per SM)
   int batch;
   int num_sms;
   cudaStream_t stream;
@@ -41,11 +43,12 @@ cudaError_t launch_combine_d256(const CombineArgs& a, int dtype, cudaStream_t st
 struct KvAppendArgs {
   const uint4* k_new;   // [B][Hkv][D] as 16-byte chunks
   const uint4* v_new;
-  const int32_t* positions;
+  const int32_t* positions;  // position of sequence b's new row: positions[b] + pos_offset
   const int32_t* page_table;
   uint4* k_pages;       // [P][PS][Hkv][D] as 16-byte chunks
   uint4* v_pages;
   int32_t* err;
+  int32_t pos_offset;
   int32_t B, Hkv, chunks, page_size, max_pages, num_pages;
 };
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t stream);

@@ -33,7 +33,6 @@ struct MmaCfg {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kRingBytes + 1024;
-  static constexpr int kChunkBytes = kTile * 128;  // one [64 tok][64 dims] sub-tile
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -58,24 +57,40 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Byte offset of (token row t, dim d) inside a swizzled [D/64][64][64] tile.
-__device__ __forceinline__ uint32_t swz_offset(int t, int d) {
-  return (uint32_t)((d >> 6) * (kTile * 128) + t * 128 + ((((d >> 3) & 7) ^ (t & 7)) << 4));
+// Byte offset of (row t, dim d) inside a swizzled tile made of pieces of
+// 2^ps rows, one TMA box each, laid out [D/64][2^ps rows][64 dims] (the
+// 128-byte swizzle: 16-byte chunk c of row t at c ^ (t % 8)).  A tile that is
+// one piece (2^ps = its rows) is [D/64][rows][64].
+template <int D>
+__device__ __forceinline__ uint32_t swz_offset(int t, int d, int ps) {
+  const int bt = 1 << ps;
+  return (uint32_t)((t >> ps) * (bt * D * 2) + (d >> 6) * (bt * 128) + (t & (bt - 1)) * 128 +
+                    ((((d >> 3) & 7) ^ (t & 7)) << 4));
 }
+
+struct NoRelease {
+  __device__ void operator()() const {}
+};
 
 // One consumer warp's 16 positions [tok0, tok0 + 16) of a staged tile:
 // scores^T = K . Q^T, the per-column causal / window mask, the online
-// softmax update and out^T += V^T . P^T.  kt points at the stage's K tile
-// (V follows at kTileBytes); [lo, hi) is the union of the columns' ranges
-// clipped to the shard, and the block must overlap it.
-template <int D, int NT8, class E>
+// softmax update and out^T += V^T . P^T.  kt points at the stage's K tile of
+// kRows rows in pieces of 2^ps rows (swz_offset), the warp's 16 rows at
+// 16 * warp (V follows at kRows * D * 2 bytes); [lo, hi) is the union of the
+// columns' ranges clipped to the shard, and the block must overlap it.  kFetchFirst: all of
+// the warp's K and V fragments are loaded into registers first and
+// release() is called before any arithmetic, so the stage can be refilled
+// while the warp computes (the same operations in the same order).
+template <int D, int NT8, class E, int kRows = kTile, bool kFetchFirst = false,
+          class Release = NoRelease>
 __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int tok0, int lo,
                                           int hi, const int (&col_lo)[NT8][2],
                                           const int (&col_hi)[NT8][2],
                                           const uint32_t (&qf)[NT8][D / 16][2], float scale_log2,
                                           float (&acc)[D / 16][NT8][4], float (&m_run)[NT8][2],
-                                          float (&l_part)[NT8][2]) {
-  using C = MmaCfg<D>;
+                                          float (&l_part)[NT8][2], int ps,
+                                          Release release = {}) {
+  constexpr int kTileBytes = kRows * D * 2;
   constexpr int KS = D / 16;
   const int gid = lane >> 2;
   const int mat = lane >> 3, mrow = lane & 7;
@@ -84,31 +99,62 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
   const int v_tok = 16 * warp + mrow + ((mat & 2) ? 8 : 0);  // V: matrix bit 1 -> +8 tokens
   const int v_dof = (mat & 1) ? 8 : 0;                       // V: matrix bit 0 -> +8 dims
   const uint32_t kbase = smem_u32(kt);
-  const uint32_t vbase = kbase + C::kTileBytes;
+  const uint32_t vbase = kbase + kTileBytes;
   if (tok0 < lo || tok0 + 16 > hi) {
     // rows of this block outside the range: clear their V rows so a
     // zero weight never meets a non-finite cache value
-    uint8_t* vt = kt + C::kTileBytes;
+    uint8_t* vt = kt + kTileBytes;
     for (int e = lane; e < 16 * (D / 8); e += 32) {
       const int t = e / (D / 8), c = e % (D / 8);
       const int tok = tok0 + t;
       if (tok < lo || tok >= hi)
-        *reinterpret_cast<uint4*>(vt + swz_offset(16 * warp + t, c * 8)) =
+        *reinterpret_cast<uint4*>(vt + swz_offset<D>(16 * warp + t, c * 8, ps)) =
             make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     __syncwarp();
   }
+  constexpr int kHeld = kFetchFirst ? KS : 1;
+  uint32_t kf[kHeld][4], vf[kHeld][4];
+  if constexpr (kFetchFirst) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+      ldmatrix_x4(kf[ks], kbase + swz_offset<D>(k_tok, ks * 16 + k_dof, ps));
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi)
+      ldmatrix_x4_trans(vf[mi], vbase + swz_offset<D>(v_tok, mi * 16 + v_dof, ps));
+    release();
+  }
   // scores^T = K . Q^T
   float sc[NT8][4];
 #pragma unroll
   for (int j = 0; j < NT8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+  if constexpr (kFetchFirst) {
+    // two independent accumulation chains (even and odd k-steps), added at
+    // the end: half the dependent mma latency on the warp's critical path
+    float sc1[NT8][4];
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t af[4];
-    ldmatrix_x4(af, kbase + swz_offset(k_tok, ks * 16 + k_dof));
+    for (int j = 0; j < NT8; ++j) sc1[j][0] = sc1[j][1] = sc1[j][2] = sc1[j][3] = 0.f;
 #pragma unroll
-    for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
+    for (int ks = 0; ks < KS; ks += 2) {
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) {
+        ElemOps<E>::mma(sc[j], kf[ks], qf[j][ks][0], qf[j][ks][1]);
+        ElemOps<E>::mma(sc1[j], kf[ks + 1], qf[j][ks + 1][0], qf[j][ks + 1][1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[j][e] += sc1[j][e];
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t af[4];
+      ldmatrix_x4(af, kbase + swz_offset<D>(k_tok, ks * 16 + k_dof, ps));
+#pragma unroll
+      for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
+    }
   }
   // online softmax over this block's 16 positions
   const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
@@ -165,7 +211,11 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
 #pragma unroll
   for (int mi = 0; mi < KS; ++mi) {
     uint32_t af[4];
-    ldmatrix_x4_trans(af, vbase + swz_offset(v_tok, mi * 16 + v_dof));
+    if constexpr (kFetchFirst) {
+      af[0] = vf[mi][0], af[1] = vf[mi][1], af[2] = vf[mi][2], af[3] = vf[mi][3];
+    } else {
+      ldmatrix_x4_trans(af, vbase + swz_offset<D>(v_tok, mi * 16 + v_dof, ps));
+    }
 #pragma unroll
     for (int j = 0; j < NT8; ++j) {
       ElemOps<E>::mma(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
@@ -303,7 +353,7 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     if (lane == 0 && !bad) {
       prefetch_tensormap(&tmap_k);
       prefetch_tensormap(&tmap_v);
-      const uint32_t box_bytes = box_t * 128;  // one 64-dim slice of box_t rows
+      const uint32_t box_bytes = box_t * D * 2;  // one piece: box_t rows, all D dims
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % C::kStages;
@@ -326,11 +376,15 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
           const int pool_rows = a.num_pages * a.page_size;
           if (!PGD_IN(coord == pool_rows ? 0 : (int64_t)coord + box_t - 1, pool_rows, a.err))
             coord = pool_rows;
+          if (box_t < kTile) {  // one box holds the piece's D dims
+            tma_load_4d(kdst + pc * box_bytes, &tmap_k, 0, coord, h, 0, fb);
+            tma_load_4d(vdst + pc * box_bytes, &tmap_v, 0, coord, h, 0, fb);
+          } else {  // 64-row pieces: one box per 64-dim chunk
 #pragma unroll
-          for (int dc = 0; dc < D / 64; ++dc) {
-            const uint32_t off = dc * C::kChunkBytes + pc * box_bytes;
-            tma_load_4d(kdst + off, &tmap_k, 0, dc, h, coord, fb);
-            tma_load_4d(vdst + off, &tmap_v, 0, dc, h, coord, fb);
+            for (int dc = 0; dc < D / 64; ++dc) {
+              tma_load_4d(kdst + dc * (kTile * 128), &tmap_k, 0, coord, h, dc, fb);
+              tma_load_4d(vdst + dc * (kTile * 128), &tmap_v, 0, coord, h, dc, fb);
+            }
           }
         }
         issued = i + 1;
@@ -344,6 +398,7 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   // ------------------------------------------------------------ consumers
   const int G = a.G;
   const int gid = lane >> 2, tig = lane & 3;
+  const int piece_shift = __ffs(box_t) - 1;  // a stage is pieces of box_t rows
   // Q^T operand fragments, held for the whole shard
   const int R = a.T * G;  // query rows of the group: r = t * G + g
   uint32_t qf[NT8][KS][2];
@@ -400,7 +455,7 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     const int tok0 = shard_lo + i * kTile + 16 * warp;  // this warp's 16 positions
     if (tok0 + 16 > lo && tok0 < hi)
       mma_block<D, NT8, E>(ring + st * C::kStageBytes, warp, lane, tok0, lo, hi, col_lo, col_hi,
-                           qf, a.scale_log2, acc, m_run, l_part);
+                           qf, a.scale_log2, acc, m_run, l_part, piece_shift);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }

@@ -385,3 +385,34 @@ def test_cluster_plans(pkg):
         params(pkg, batch=2, num_q_heads=64, page_size=64, max_pages_per_seq=1024,
                num_pages=2048, max_seq_len=65536, force_chunk=8192), 152)
     assert plan.max_shards == 8 and plan.cluster == 0
+
+
+def test_all_heads_plans(pkg):
+    """The all-heads schedule, on request, on the shapes its kernel serves
+    (tensor cores, D 64/128, 8 KV heads, G <= 8, T = 1, pages of 16 or more):
+    one CTA per SM, shards of 256..1024 positions; the planner never picks it
+    by itself; asking for it where it does not apply is an error."""
+    batched = dict(batch=64, max_pages_per_seq=512, num_pages=20000, max_seq_len=8192)
+    assert pkg.decode_attn_make_plan(params(pkg, **batched), 152).all_heads == 0
+    batched["schedule"] = 4
+    plan = pkg.decode_attn_make_plan(params(pkg, **batched), 152)
+    assert plan.all_heads == 1 and plan.split == 1 and plan.grid_x == 152
+    assert plan.grid_y == plan.grid_z == 1 and plan.cluster == 0 and plan.tile_tokens == 16
+    assert plan.chunk_tokens == 512 and plan.max_shards == 16 and plan.ring_stages == 3
+    tickets = max(64 * 1024, ((64 * 8 + 64) * 4 + 255) // 256 * 256)
+    assert plan.workspace_bytes == tickets + 64 * 32 * 16 * 8 + 64 * 32 * 16 * 128 * 4
+    plan = pkg.decode_attn_make_plan(params(pkg, **batched, head_dim=64), 152)
+    assert plan.all_heads == 1 and plan.ring_stages == 6
+    many = dict(batch=1000, max_pages_per_seq=32, num_pages=40000, max_seq_len=512, schedule=4)
+    plan = pkg.decode_attn_make_plan(params(pkg, **many), 152)
+    assert plan.all_heads == 1 and plan.chunk_tokens == 256 and plan.max_shards == 2
+    assert pkg.decode_attn_make_plan(params(pkg), 152).all_heads == 0            # Llama shape
+    for kw in (dict(head_dim=256), dict(num_q_heads=16, num_kv_heads=4), dict(num_queries=2),
+               dict(num_q_heads=128), dict(page_size=8, max_pages_per_seq=1024),
+               dict(force_chunk=2048), dict(variant=1)):
+        with pytest.raises(pkg.DecodeAttnError):
+            pkg.decode_attn_make_plan(params(pkg, **{**batched, **kw}), 152)
+    plan = pkg.decode_attn_make_plan(params(pkg, schedule=4), 152)   # forced on a small step
+    assert plan.all_heads == 1 and plan.max_shards == math.ceil(3060 / plan.chunk_tokens)
+    plan = pkg.decode_attn_make_plan(params(pkg, **batched, force_chunk=300), 152)
+    assert plan.chunk_tokens == 320 and plan.max_shards == math.ceil(8192 / 320)

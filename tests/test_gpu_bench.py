@@ -34,8 +34,9 @@ def gpu():
 @pytest.mark.parametrize("name", ["tiny", "llama"])
 def test_bench_line_and_dump_match_the_oracle(gpu, tmp_path, name):
     path = str(tmp_path / f"{name}.npz")
+    cpu = ["--cpu-budget", "1"] if name == "tiny" else ["--no-cpu-baseline"]
     (line,) = run_bench("--workload", name, "--steps", "5", "--warmup", "3", "--e2e-steps", "0",
-                        "--no-cpu-baseline", "--dump", path)
+                        *cpu, "--dump", path)
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -44,6 +45,13 @@ def test_bench_line_and_dump_match_the_oracle(gpu, tmp_path, name):
     roof = line["roofline"]
     assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    for pc in (roof["launch_us_percentiles"], line["step_us_percentiles"]):
+        assert 0 < pc["p10"] <= pc["p50"] <= pc["p90"]
+    if name == "tiny":
+        cb = line["cpu_baseline"]
+        assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["cpu"]
+        if cb["cores"] > 1:
+            assert cb["one_thread"]["value"] > 0
     d = np.load(path)
     assert str(d["workload"]) == name and json.loads(str(d["plan"]))["variant"] == 2
     # the workloads draw from the device's own generator: regenerate on the

@@ -447,9 +447,9 @@ def test_dirty_workspace_is_detected_and_clearable(pkg):
     (128, 32, 8, torch.float16, 0), (128, 32, 8, torch.bfloat16, 100),
     (64, 32, 8, torch.float16, 0), (64, 64, 4, torch.float16, 37)])
 def test_shallow_ring_parity(pkg, D, Hq, Hkv, dt, window):
-    """Several waves of one-shard CTAs (400 sequences of 0..512 tokens) run
-    the 2-stage (4 at D=64) ring, 3 CTAs per SM; against the oracle, and
-    bitwise run to run."""
+    """Several waves of one-shard CTAs (400 sequences of 0..512 tokens) on
+    the grid schedule run the 2-stage (4 at D=64) ring, 3 CTAs per SM;
+    against the oracle, and bitwise run to run."""
     g = torch.Generator().manual_seed(90 + D + Hq)
     lens = torch.randint(1, 513, (400,), generator=g)
     lens[::53] = 1
@@ -457,11 +457,11 @@ def test_shallow_ring_parity(pkg, D, Hq, Hkv, dt, window):
                               head_dim=D, page_size=16, seq_lens=lens, seed=91, dtype=dt,
                               device=DEV)
     w.seq_lens[7] = 0
-    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, window, 512)
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, window, 512, schedule=1)
     plan = pkg.decode_attn_make_plan(params,
                                      torch.cuda.get_device_properties(DEV).multi_processor_count)
     assert plan.ring_stages == (4 if D == 64 else 2)
-    out, err = run(pkg, w, window=window, max_seq_len=512)
+    out, err = run(pkg, w, window=window, max_seq_len=512, schedule=1)
     assert err == 0
     ref = oracle_of(w, window=window)
     if dt == torch.bfloat16:
@@ -469,7 +469,7 @@ def test_shallow_ring_parity(pkg, D, Hq, Hkv, dt, window):
         assert rel <= 3e-3 and mab <= 1e-2 and rrel <= 6e-3, (rel, mab, rrel)
     else:
         assert_parity(out, ref)
-    again, _ = run(pkg, w, window=window, max_seq_len=512)
+    again, _ = run(pkg, w, window=window, max_seq_len=512, schedule=1)
     assert torch.equal(out, again)
     assert torch.all(out[7] == 0)
 
