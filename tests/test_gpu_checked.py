@@ -2,7 +2,8 @@
 and TMA coordinate range-checked in the kernels; a violation raises
 DECODE_ATTN_DEV_CHECK and skips the access).  A memory checker cannot run
 on these GPUs, so this is how an out-of-range access would show: the suites
-assert that no device error bit is set on valid inputs."""
+assert that no device error bit is set on valid inputs (the two tests that
+time a pipeline out on purpose are left out)."""
 import os
 import subprocess
 import sys
@@ -14,7 +15,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_append.py", "tests/test_gpu_multi.py",
           "tests/test_gpu_bf16.py", "tests/test_gpu_persistent.py", "tests/test_gpu_cluster.py",
-          "tests/test_gpu_poison.py"]
+          "tests/test_gpu_poison.py", "tests/test_gpu_all_heads.py"]
 
 
 def test_gpu_suites_pass_on_the_checked_build():
@@ -30,7 +31,7 @@ def test_gpu_suites_pass_on_the_checked_build():
     assert probe.returncode == 0, probe.stderr[-2000:]
     assert probe.stdout.strip().endswith("libpaged_gqa_decode_checked.so")
     r = subprocess.run([sys.executable, "-m", "pytest", "-m", "gpu", "-x", "-q",
-                        "-p", "no:cacheprovider", *SUITES, "-k", "not stalled"],
+                        "-p", "no:cacheprovider", *SUITES, "-k", "not stall"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=3000)
     assert r.returncode == 0, r.stdout[-4000:]
     assert " passed" in r.stdout
