@@ -453,15 +453,16 @@ int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params
 // of 16) went from 197.2 to 193-195 us with the whole piece in one box.
 // 64-row pieces keep one box per 64-dim chunk (8 KB each), which measured
 // faster there (one 131072-token sequence 89.1 against 90.2 us).
-int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_attn_params* p,
-                             int box_t) {
+int encode_pool_map_swizzled_boxes(CUtensorMap* map, const void* base,
+                                   const decode_attn_params* p, int box_t, bool per_chunk) {
   auto fn = encode_fn();
   if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
   const int D = p->head_dim;
   cuuint64_t dims[4] = {64, (cuuint64_t)p->num_pages * p->page_size,
                         (cuuint64_t)p->num_kv_heads, (cuuint64_t)D / 64};
   cuuint64_t strides[3] = {(cuuint64_t)p->num_kv_heads * D * 2, (cuuint64_t)D * 2, 128};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_t, 1, box_t < kTile ? (cuuint32_t)D / 64 : 1u};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_t, 1,
+                       (box_t < kTile && !per_chunk) ? (cuuint32_t)D / 64 : 1u};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -470,6 +471,18 @@ int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_at
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
+}
+
+int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_attn_params* p,
+                             int box_t) {
+  return encode_pool_map_swizzled_boxes(map, base, p, box_t, false);
+}
+
+// The persistent kernel's view: one box per (piece, 64-dim chunk), its
+// stages laid out [D/64][64 rows][64] as one piece.
+int encode_pool_map_chunks(CUtensorMap* map, const void* base, const decode_attn_params* p,
+                           int box_t) {
+  return encode_pool_map_swizzled_boxes(map, base, p, box_t, true);
 }
 
 // 4-D view (64 dims, P*PS token rows, kv head, D/64 chunks) with the 128-byte
@@ -549,7 +562,8 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   if (p->batch == 0) return DECODE_ATTN_OK;
   SplitLaunch L{};
   const int box_t = std::min(p->page_size, kTile);
-  auto encode = plan.all_heads ? encode_pool_map_heads
+  auto encode = plan.all_heads    ? encode_pool_map_heads
+                : plan.persistent ? encode_pool_map_chunks
                 : plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
                                                            : encode_pool_map;
   int st = encode(&L.tmap_k, k_pages, p, box_t);

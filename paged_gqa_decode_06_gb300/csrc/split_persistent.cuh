@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       prefetch_tensormap(&tmap_v);
     }
     const int oob = a.num_pages * a.page_size;  // past the pool: TMA writes zeros
-    const uint32_t box_bytes = box_t * D * 2;  // one piece: box_t rows, all D dims
+    const uint32_t box_bytes = box_t * 128;  // one 64-dim slice of box_t rows
     SegWalker wk;
     wk.start(prefix_s, pa.B, hh, g0, g1);
     int it = 0, ord = 0;
@@ -265,15 +265,11 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
             const uint32_t vdst = kdst + C::kTileBytes;
             for (int pc = 0; pc < ppt; ++pc) {
               const int coord = coord_s[pt + pc];
-              if (box_t < kTile) {  // one box holds the piece's D dims
-                tma_load_4d(kdst + pc * box_bytes, &tmap_k, 0, coord, sg.h, 0, fb);
-                tma_load_4d(vdst + pc * box_bytes, &tmap_v, 0, coord, sg.h, 0, fb);
-              } else {  // 64-row pieces: one box per 64-dim chunk
 #pragma unroll
-                for (int dc = 0; dc < D / 64; ++dc) {
-                  tma_load_4d(kdst + dc * (kTile * 128), &tmap_k, 0, coord, sg.h, dc, fb);
-                  tma_load_4d(vdst + dc * (kTile * 128), &tmap_v, 0, coord, sg.h, dc, fb);
-                }
+              for (int dc = 0; dc < D / 64; ++dc) {  // one box per 64-dim chunk
+                const uint32_t off = dc * (kTile * 128) + pc * box_bytes;
+                tma_load_4d(kdst + off, &tmap_k, 0, coord, sg.h, dc, fb);
+                tma_load_4d(vdst + off, &tmap_v, 0, coord, sg.h, dc, fb);
               }
             }
           }
@@ -357,8 +353,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
       }
       const int tok0 = seg_lo + k * kTile + 16 * warp;
       if (tok0 + 16 > lo && tok0 < hi)
+        // per-chunk boxes: the stage is one piece of 64 rows
         mma_block<D, NT8, E>(ring + st * C::kStageBytes, warp, lane, tok0, lo, hi, col_lo,
-                             col_hi, qf, a.scale_log2, acc, m_run, l_part, __ffs(box_t) - 1);
+                             col_hi, qf, a.scale_log2, acc, m_run, l_part, 6);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
     }
