@@ -233,6 +233,21 @@ def recorded_traffic(workload: str):
 
 # ------------------------------------------------------------ CPU oracle
 
+def split_kernel_name(plan, head_dim: int) -> str:
+    """The split kernel a plan launches (the one the roofline is taken on)."""
+    if plan.variant == 1:
+        return "split_simt_kernel"
+    if plan.all_heads:
+        return "split_allheads_kernel"
+    if plan.persistent:
+        return "split_mma_persistent_kernel"
+    if plan.cluster > 0:
+        return "split_mma_kernel_cluster"
+    if plan.ring_stages == (4 if head_dim == 64 else 2):
+        return "split_mma_kernel_shallow"
+    return "split_mma_kernel"
+
+
 def cpu_model() -> str:
     """The host CPU's name from /proc/cpuinfo (x86 'model name'; on Arm the
     implementer/part codes when no name is given)."""
@@ -530,9 +545,7 @@ def gpu_arm(args):
                        "l2": ("flushed between timed steps (write of 4x L2, then read of 4x L2)" if flush else
                               f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"),
                        "plan": plan.as_dict(), "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "split_simt_kernel" if plan.variant == 1
-                         else "split_allheads_kernel" if plan.all_heads
-                         else "split_mma_kernel",
+            "roofline": {"bound": "hbm", "kernel": split_kernel_name(plan, w.head_dim),
                          "achieved": split_achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": split_achieved_gbs / peak_gbs, "peak_source": peak_src,
                          "traffic": traffic,
