@@ -228,7 +228,9 @@ int decode_kv_append(const decode_attn_params* p, const void* k_new, const void*
  * position; sequences with seq_len 0 get no row) followed by decode_attn.
  * The CTA holding each sequence's last position writes the new rows of its
  * KV head before it streams its tiles.  Arguments as decode_attn plus k_new,
- * v_new ([B][Hkv][D] fp16 device); k_pages and v_pages are written.
+ * v_new ([B][Hkv][D] fp16 device); k_pages and v_pages are written.  On an
+ * all-heads plan (DECODE_ATTN_SCHEDULE_ALL_HEADS) the append runs as its own
+ * kernel just before the attention launch (two launches, same result).
  */
 int decode_attn_append(const decode_attn_params* p, const void* q, const void* k_new,
                        const void* v_new, void* k_pages, void* v_pages,
