@@ -12,9 +12,11 @@
 // tile) so the weights keep about twice the element format's bits (22 for
 // fp16, 16 for bf16).  Templated on the element format E (fp16 or bf16).
 //
-// Shared-memory tiles are [D/64][64 tokens][64 dims] with the 128-byte TMA
-// swizzle (16-byte chunk c of token row t lives at chunk c ^ (t % 8)), so
-// every ldmatrix of 8 token rows touches 8 distinct bank groups.
+// A stage's K (and V) tile is 64 tokens made of pieces of box_t = min(page,
+// 64) rows, one TMA box each, every piece laid out [D/64][box_t rows][64
+// dims] with the 128-byte TMA swizzle (16-byte chunk c of token row t lives
+// at chunk c ^ (t % 8)), so every ldmatrix of 8 token rows touches 8
+// distinct bank groups (swz_offset).
 #pragma once
 
 #include "split_simt.cuh"  // SplitArgs, zero_group_rows
