@@ -128,7 +128,10 @@ def make_params(q, k_pages, page_table, scale: float, window: int = 0,
     """Parameters from tensor shapes: q [B,Hq,D] (or [B,T,Hq,D] for T query
     positions per sequence), k_pages [P,PS,Hkv,D], page_table [B,maxPages].
     ``max_seq_len`` is a host-side bound on seq_lens (it sizes the grid;
-    None = the page table's capacity)."""
+    None = the page table's capacity).  ``schedule``: SCHEDULE_AUTO (the
+    planner's grid or cluster plan), SCHEDULE_GRID, SCHEDULE_PERSISTENT,
+    SCHEDULE_CLUSTER or SCHEDULE_ALL_HEADS (the last three on request only;
+    a schedule the shape cannot take raises DecodeAttnError at planning)."""
     if len(q.shape) == 4:
         B, T, Hq, D = q.shape
     else:
