@@ -78,6 +78,8 @@ def parse_args(argv=None):
     ap.add_argument("--dump", default="",
                     help="write the step's output (fp32), the workload and the plan to this "
                          ".npz for offline comparison with the oracle")
+    ap.add_argument("--config-steps", type=int, default=200,
+                    help="timed steps of each per_config entry (0 skips the block)")
     ap.add_argument("--context-sweep", action="store_true",
                     help="threshold A/B instead of the bench line: contexts 1..512 of the "
                          "three head-dim shapes, split threshold 256 (default), always split, "
@@ -337,6 +339,85 @@ class OracleSample:
 
 # ------------------------------------------------------------ GPU arm
 
+# The configurations the per_config block times besides the headline (every
+# workload of the benchmark's config list: the tiny decode, the Llama-3.1-8B
+# shape, the head_dim sweep at 3060 tokens, the batched serving mix and the
+# long context with a 4096-position window).
+PER_CONFIG = ("tiny", "llama", "sweep_d64", "sweep_d128", "sweep_d256", "batched",
+              "long_w4096")
+
+
+def l2_policy(kv_bytes: int, l2_bytes: int):
+    """(flush?, description): steps whose K/V fit in twice the L2 flush it
+    between timed steps; larger inputs stream from HBM anyway."""
+    if kv_bytes < 2 * l2_bytes:
+        return True, "flushed between timed steps (write of 4x L2, then read of 4x L2)"
+    return False, f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"
+
+
+def time_config(pkg, workloads, name, dev, local, steps, dtype, peak_gbs, flush_l2, l2):
+    """One per_config entry: the workload's decode step (decode_attn_split,
+    one launch) captured in a CUDA graph and replayed `steps` times, each
+    replay bracketed by events on the launching stream, L2 flushed before each
+    step when the workload fits in twice the L2."""
+    import torch
+    w = workloads.make(name, device=dev, dtype=dtype)
+    kv_bytes = w.kv_bytes()
+    max_len = w.max_seq_len()
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, w.window, max_len)
+    props = torch.cuda.get_device_properties(dev)
+    plan = pkg.decode_attn_make_plan(params, props.multi_processor_count)
+    ws = torch.zeros(max(pkg.decode_attn_workspace_size(params, local), 256), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty_like(w.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush, l2_desc = l2_policy(kv_bytes, l2)
+
+    def step():
+        pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                              window=w.window, out=out, max_seq_len=max_len, workspace=ws,
+                              err_flag=err)
+
+    for _ in range(3):
+        if flush:
+            flush_l2()
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        if flush:
+            flush_l2()
+        g.replay()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        if flush:
+            flush_l2()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"{name}: device error bits {int(err.item())}")
+    mean_ms = statistics.mean(ms)
+    gbs = kv_bytes / (mean_ms * 1e-3) / 1e9
+    entry = {"desc": WORKLOAD_DESC[name], "us_per_step": mean_ms * 1e3,
+             "us_percentiles": percentiles_us(ms), "kv_bytes_per_step": kv_bytes,
+             "kv_tbs": gbs / 1e3, "frac": gbs / peak_gbs, "steps": steps, "l2": l2_desc,
+             "kernel": split_kernel_name(plan, w.head_dim),
+             "plan": {k: plan.as_dict()[k] for k in ("split", "chunk_tokens", "max_shards",
+                                                     "grid_x", "grid_y", "grid_z", "cluster",
+                                                     "ring_stages")}}
+    del g, w, ws, out
+    torch.cuda.empty_cache()
+    return entry
+
+
 def gpu_arm(args):
     import torch
     import paged_gqa_decode_06_gb300 as pkg
@@ -380,9 +461,9 @@ def gpu_arm(args):
     stream = torch.cuda.current_stream(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     resident = (w.k_pages.numel() + w.v_pages.numel()) * 2
-    flush = kv_bytes < 2 * l2
-    flush_buf = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev) if flush else None
-    flush_read = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev) if flush else None
+    flush, l2_desc = l2_policy(kv_bytes, l2)
+    flush_buf = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_read = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
 
     def flush_l2():
         # write 4x L2 (evicts the step's data), then read another 4x L2 so the
@@ -484,6 +565,16 @@ def gpu_arm(args):
     peak_gbs, peak_src = load_peak_hbm()
     split_achieved_gbs = kv_bytes / (split_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
+    # ---- every other configuration of the benchmark, timed the same way
+    per_config = None
+    if rank == 0 and args.config_steps > 0 and T == 1 and not args.append and \
+            args.variant == 0 and args.schedule == 0 and args.force_chunk == 0:
+        per_config = {}
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            per_config[name] = time_config(pkg, workloads, name, dev, local, args.config_steps,
+                                           edt, peak_gbs, flush_l2, l2)
     # ---- end to end from pinned host buffers through the C ABI
     e2e = None
     if args.e2e_steps > 0 and T == 1 and not args.append:
@@ -542,9 +633,8 @@ def gpu_arm(args):
             "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload],
                        "queries_per_seq": T, "fused_append": bool(args.append),
                        "kv_bytes_per_step": kv_bytes, "resident_kv_bytes": resident,
-                       "l2": ("flushed between timed steps (write of 4x L2, then read of 4x L2)" if flush else
-                              f"inputs {kv_bytes / 2**30:.2f} GiB > L2, no flush"),
-                       "plan": plan.as_dict(), "parallelism": f"replicas x{world}"},
+                       "l2": l2_desc, "parallelism": f"replicas x{world}"},
+            "plan": plan.as_dict(),
             "roofline": {"bound": "hbm", "kernel": split_kernel_name(plan, w.head_dim),
                          "achieved": split_achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": split_achieved_gbs / peak_gbs, "peak_source": peak_src,
@@ -553,7 +643,7 @@ def gpu_arm(args):
                          "launch_us": split_avg_ms * 1e3,
                          "launch_us_percentiles": percentiles_us(split_ms)},
             "step_us_percentiles": percentiles_us(step_ms) if step_ms else None,
-            "cpu_baseline": cpu, "e2e": e2e,
+            "cpu_baseline": cpu, "e2e": e2e, "per_config": per_config,
             "gpu_launches": K,
             "launch_mode": "eager" if args.eager else "cuda graph replay",
             "clocks": clocks,
@@ -648,6 +738,12 @@ def reference_arm(args):
     import oracle
     oracle.build()
     w = workloads.make(args.workload, device="cpu")
+    kv_bytes = w.kv_bytes()
+    resident = (w.k_pages.numel() + w.v_pages.numel()) * 2
+    # the GPU arm's L2 rule, so both arms name the same configuration
+    l2 = 126 << 20
+    if torch.cuda.is_available():
+        l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", l2) or l2
     cores = cpu_cores()
     steps = args.steps + args.warmup
     per_step = max(0.02, min(5.0, 120.0 / steps))
@@ -667,7 +763,10 @@ def reference_arm(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) fp16)",
         "impl": "reference",
-        "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload]},
+        "config": {"workload": args.workload, "desc": WORKLOAD_DESC[args.workload],
+                   "queries_per_seq": 1, "fused_append": False,
+                   "kv_bytes_per_step": kv_bytes, "resident_kv_bytes": resident,
+                   "l2": l2_policy(kv_bytes, l2)[1], "parallelism": f"replicas x{world}"},
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
                          "sample": f"per step: {desc}", "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,

@@ -280,9 +280,12 @@ const char* decode_attn_strerror(int status);
  * DECODE_ATTN_ERR_SCRATCH_LIMIT without launching; decode_attn_workspace_size
  * tells the need in advance.  All calls on a device share the array: calls
  * whose GPU work can overlap (other streams, other host threads) race and
- * must be serialised by the caller.  The array starts zeroed, and every
- * completed call leaves the shard tickets it keeps there at zero; nothing
- * needs clearing by the caller.  Calls no cudaMalloc, cudaFree or allocating routine.
+ * must be serialised by the caller.  The array keeps the last call's
+ * contents; the only part that must start at zero, the shard tickets, is
+ * cleared by each call itself (an asynchronous memset on `stream` before the
+ * launch), so nothing needs clearing by the caller, also after a call that
+ * reported DECODE_ATTN_DEV_TIMEOUT.  Calls no cudaMalloc, cudaFree or
+ * allocating routine.
  */
 #define DECODE_ATTN_STATIC_SCRATCH_BYTES (8u << 20)
 #define DECODE_ATTN_ERR_SCRATCH_LIMIT (-11) /* partials above the static scratch size */

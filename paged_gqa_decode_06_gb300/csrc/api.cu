@@ -123,6 +123,7 @@ int next_pow2(int x) {
 }  // namespace
 
 namespace pgd {
+int validate_params(const decode_attn_params* p) { return check_params(p); }
 size_t simt_smem_bytes(int head_dim) {
   switch (head_dim) {
     case 64: return SimtCfg<64>::kSmemBytes;

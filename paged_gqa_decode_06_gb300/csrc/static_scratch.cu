@@ -18,17 +18,25 @@
 // routine is used here.
 //
 // Every call on a device shares the one array and leaves its contents behind.
-// The only part that must start at zero, the per-group shard tickets, starts
-// zeroed (a __device__ array is zero-initialised at module load) and every
-// completed call leaves it zero again; every partial the merge reads is
-// written earlier in the same call.  Calls
-// whose work overlaps on the GPU (different streams, or different host
-// threads) race on the array and must be serialised by the caller.
+// The only part that must start at zero, the per-group shard tickets, is
+// cleared by each call itself: before its launch, an asynchronous memset on
+// the call's stream zeroes the array's ticket region (a memset allocates
+// nothing).  So a call that ended early (a pipeline wait that gave up) cannot
+// leave a stale ticket for the next one.  Every partial the merge reads is
+// written earlier in the same call.  Calls whose work overlaps on the GPU
+// (different streams, or different host threads) race on the array and must
+// be serialised by the caller.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/decode_attn.h"
+
+namespace pgd {
+// The argument checks decode_attn_make_plan starts with (api.cu): shapes,
+// head dim, page size, group, dtype, schedule; no device call.
+int validate_params(const decode_attn_params* p);
+}  // namespace pgd
 
 namespace {
 
@@ -58,10 +66,8 @@ extern "C" int decode_attn_static_scratch(const decode_attn_params* p, const voi
                                           const void* k_pages, const void* v_pages,
                                           const int32_t* page_table, const int32_t* seq_lens,
                                           void* out, int32_t* err_flag, void* stream) {
-  decode_attn_plan plan;
-  // argument errors first, without touching the device (an SM count large
-  // enough that no schedule is refused for it; the real plan follows)
-  int st = decode_attn_make_plan(p, 1 << 16, &plan);
+  // argument errors first, without touching the device
+  int st = pgd::validate_params(p);
   if (st) return st;
   int device = 0, sms = 0;
   if (cudaGetDevice(&device) != cudaSuccess ||
@@ -69,8 +75,12 @@ extern "C" int decode_attn_static_scratch(const decode_attn_params* p, const voi
     return DECODE_ATTN_ERR_CUDA;
   void* scratch = nullptr;
   if ((st = scratch_address(device, &scratch))) return st;  // set-up on the first call
+  decode_attn_plan plan;
   if ((st = decode_attn_make_plan(p, sms, &plan))) return st;
   if (plan.workspace_bytes > DECODE_ATTN_STATIC_SCRATCH_BYTES) return DECODE_ATTN_ERR_SCRATCH_LIMIT;
+  // the tickets of this call start at zero whatever the last call left
+  if ((st = decode_attn_workspace_clear(p, scratch, DECODE_ATTN_STATIC_SCRATCH_BYTES, stream)))
+    return st;
   return decode_attn(p, q, k_pages, v_pages, page_table, seq_lens, out, scratch,
                      DECODE_ATTN_STATIC_SCRATCH_BYTES, err_flag, stream);
 }

@@ -84,6 +84,22 @@ def test_bad_params_rejected_before_launch(pkg, field, value, code):
                            nul) == code
 
 
+@pytest.mark.parametrize("field,value,code", [
+    ("head_dim", 96, -3), ("page_size", 24, -4), ("num_q_heads", 30, -2),
+    ("num_q_heads", 8 * 32, -5), ("scale", float("inf"), -2),
+])
+def test_static_scratch_rejects_bad_params_without_a_device(pkg, field, value, code):
+    # the no-allocation entry point checks its arguments with the planner's
+    # parameter checks before any CUDA call (no plan at a made-up SM count)
+    lib = pkg.load_library()
+    f = lib.decode_attn_static_scratch
+    f.argtypes = [ctypes.POINTER(pkg.DecodeAttnParams)] + [ctypes.c_void_p] * 8
+    f.restype = ctypes.c_int
+    p = params(pkg, **{field: value})
+    assert f(ctypes.byref(p), *([None] * 8)) == code
+    assert f(None, *([None] * 8)) == -1
+
+
 def test_null_params(pkg):
     lib = pkg.load_library()
     assert lib.decode_attn(None, None, None, None, None, None, None, None, 0, None, None) == -1

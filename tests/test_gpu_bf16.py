@@ -113,12 +113,10 @@ def test_bf16_multi_query_and_fused_append(pkg):
     check(out, ref)
 
 
-def test_bf16_long_context_sampled_rows(pkg):
+def test_bf16_long_context_all_rows(pkg):
     w = workloads.make("long", device=DEV, dtype=BF)
     out = run(pkg, w)
-    Hq = w.num_q_heads
-    rows = np.array([b * Hq + hq for b in range(w.batch) for hq in (0, 21, 42, 63)])
     wc = w.to("cpu")
     ref = oracle.decode_attn(wc.q, wc.k_pages, wc.v_pages, wc.page_table, wc.seq_lens, wc.scale,
-                             0, rows=rows)
-    check(out, ref, rows=rows)
+                             0)
+    check(out, ref)

@@ -6,13 +6,20 @@ partials live in the library's fixed device array instead of a workspace.
 
 Checked through the C ABI against decode_attn with a caller workspace, on two
 calls in a row (the second call finds the first call's partials still in the
-array), within the parity tolerance the other GPU tests use.  This file is
-collected last so that a run stopping at the first failure has already run
-every other test; it also passes alone in a fresh process."""
+array).  Both entry points make the same plan and launch the same kernel, so
+their outputs must agree bit for bit; the output is also compared with the
+f64 oracle at the parity tolerance the other GPU tests use.  A call whose
+pipeline wait gives up must not spoil the next one: each call clears the
+array's shard tickets itself.  This file is collected last so that a run
+stopping at the first failure has already run every other test; it also
+passes alone in a fresh process."""
+import os
+
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_gqa_decode_06_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -27,16 +34,27 @@ def pkg():
         pytest.skip("no CUDA device")
     from paged_gqa_decode_06_gb300 import build
     build.build()
+    oracle.build()
     import paged_gqa_decode_06_gb300 as p
     p.load_library()
     return p
 
 
-def _close(a, b):
-    x = a.float().cpu().numpy().astype(np.float64)
-    y = b.float().cpu().numpy().astype(np.float64)
-    rel = np.linalg.norm(x - y) / max(np.linalg.norm(y), 1e-30)
-    return rel <= REL_L2 and np.abs(x - y).max() <= MAX_ABS
+def _assert_close_to_oracle(out, w):
+    wc = w.to("cpu")
+    ref = oracle.decode_attn(wc.q, wc.k_pages, wc.v_pages, wc.page_table, wc.seq_lens, wc.scale,
+                             w.window)
+    x = out.float().cpu().numpy().astype(np.float64).reshape(ref.shape)
+    rel = np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel <= REL_L2 and np.abs(x - ref).max() <= MAX_ABS, (w.name, rel)
+
+
+def _static(pkg, w, err):
+    out = torch.empty_like(w.q)
+    pkg.decode_attn_static_scratch(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
+                                   w.scale, window=w.window, out=out, max_seq_len=w.max_seq_len(),
+                                   err_flag=err)
+    return out
 
 
 @pytest.mark.parametrize("name", ["llama", "long_w4096", "batched"])
@@ -48,17 +66,35 @@ def test_static_scratch_matches_workspace_path(pkg, name):
     ref = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
                           window=w.window, max_seq_len=L)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    outs = []
-    for _ in range(2):
-        out = torch.empty_like(w.q)
-        pkg.decode_attn_static_scratch(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
-                                       w.scale, window=w.window, out=out, max_seq_len=L,
-                                       err_flag=err)
-        outs.append(out)
+    outs = [_static(pkg, w, err) for _ in range(2)]
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     for out in outs:
-        assert _close(out, ref)
+        assert torch.equal(out, ref)
+    _assert_close_to_oracle(outs[1], w)
+
+
+def test_static_scratch_after_a_call_that_gave_up(pkg):
+    """A call whose consumers' first wait runs out (the library's
+    DECODE_ATTN_TEST_STALL_TX hook makes the first stage expect more bytes
+    than arrive) reports DECODE_ATTN_DEV_TIMEOUT; the next call on the
+    shared array must again equal decode_attn bit for bit, with no error."""
+    w = workloads.make("llama", device=DEV)
+    ref = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                          max_seq_len=w.max_seq_len())
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    os.environ["DECODE_ATTN_TEST_STALL_TX"] = "64"
+    try:
+        _static(pkg, w, err)
+        torch.cuda.synchronize()
+    finally:
+        del os.environ["DECODE_ATTN_TEST_STALL_TX"]
+    assert int(err.item()) & pkg.DEV_TIMEOUT
+    err.zero_()
+    out = _static(pkg, w, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out, ref)
 
 
 def test_static_scratch_rejects_plans_above_its_size(pkg):
