@@ -72,7 +72,7 @@ def parse_args(argv=None):
                     help="time the fused append + attention launch (new rows at the last "
                          "T positions)")
     ap.add_argument("--schedule", type=int, default=0,
-                    help="0 planner, 1 grid, 2 persistent balanced")
+                    help="0 planner, 1 grid (workspace merge), 2 cluster merge")
     ap.add_argument("--eager", action="store_true",
                     help="launch each step from the host instead of replaying a CUDA graph")
     ap.add_argument("--dump", default="",
@@ -239,10 +239,6 @@ def split_kernel_name(plan, head_dim: int) -> str:
     """The split kernel a plan launches (the one the roofline is taken on)."""
     if plan.variant == 1:
         return "split_simt_kernel"
-    if plan.all_heads:
-        return "split_allheads_kernel"
-    if plan.persistent:
-        return "split_mma_persistent_kernel"
     if plan.cluster > 0:
         return "split_mma_kernel_cluster"
     if plan.ring_stages == (4 if head_dim == 64 else 2):

@@ -64,9 +64,7 @@ extern "C" {
 #define DECODE_ATTN_DEV_BAD_LEN 1       /* seq_len < 0 or > max_pages_per_seq * page_size */
 #define DECODE_ATTN_DEV_BAD_PAGE 2      /* page id outside [0, num_pages) in an attended range */
 #define DECODE_ATTN_DEV_OVER_HINT 4     /* seq_len beyond the max_seq_len the grid was planned for */
-#define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed
-                                           (all-heads plans: the call's rows are unspecified
-                                           and the workspace must be cleared) */
+#define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed */
 #define DECODE_ATTN_DEV_CHECK 32        /* checked build only (libpaged_gqa_decode_checked.so):
                                            an index fell outside its buffer; that access was
                                            skipped (or pointed at the zero-fill coordinate) */
@@ -81,21 +79,10 @@ extern "C" {
 #define DECODE_ATTN_SCHEDULE_AUTO 0       /* planner picks (grid, or cluster where it gains) */
 #define DECODE_ATTN_SCHEDULE_GRID 1       /* one CTA per (shard, KV head, sequence); the
                                              last CTA of a group merges via the workspace */
-#define DECODE_ATTN_SCHEDULE_PERSISTENT 2 /* one CTA per resident slot, equal tile ranges
-                                             of the flattened (sequence, KV head, tile) list;
-                                             tensor-core variant, B <= 1024 */
-#define DECODE_ATTN_SCHEDULE_CLUSTER 3    /* grid schedule whose shards of one (KV head,
+#define DECODE_ATTN_SCHEDULE_CLUSTER 2    /* grid schedule whose shards of one (KV head,
                                              sequence) form a thread-block cluster and merge
                                              through distributed shared memory; one-wave
-                                             split plans of 2..8 shards, tensor-core variant */
-#define DECODE_ATTN_SCHEDULE_ALL_HEADS 4  /* one persistent CTA per SM takes (sequence, shard)
-                                             items from a counter and streams 16-position
-                                             slices of all 8 KV heads per stage (whole page
-                                             rows), one consumer warp per KV head; the warp
-                                             that completes a (sequence, KV head) merges it.
-                                             Tensor-core variant, D 64 or 128, Hkv = 8,
-                                             G <= 8, T = 1, page_size >= 16; used only
-                                             when asked for */
+                                             split plans of 2..16 shards, tensor-core variant */
 
 /* Kernel variants (decode_attn_params.variant). */
 #define DECODE_ATTN_VARIANT_AUTO 0      /* planner picks */
@@ -138,17 +125,13 @@ typedef struct decode_attn_plan {
   int32_t grid_x, grid_y, grid_z;  /* split-kernel grid: (kv head, shard, batch) when
                                       head_fastest, else (shard, kv head, batch) */
   int32_t ctas_per_sm;       /* resident CTAs per SM the grid was sized for */
-  int32_t persistent;        /* 1: persistent balanced schedule (grid_x = CTAs, slots
-                                of 2 partials per CTA); 0: grid schedule */
   int32_t head_fastest;      /* grid schedule order: 1 for plans of several waves */
   int32_t ring_stages;       /* 64-token K/V stages in flight per CTA: 3 (6 at D=64);
                                 2 (4 at D=64) for grids of several waves of short
                                 shards, which fit 3 CTAs per SM (tensor-core variant) */
   int32_t cluster;           /* CTAs per thread-block cluster (the shards of one
                                 (KV head, sequence), merged through distributed shared
-                                memory), or 0 (merged through the workspace) */
-  int32_t all_heads;         /* 1: the all-heads schedule (grid_x = SMs, one CTA each;
-                                tile_tokens = 16 positions per stage of all KV heads) */
+                                memory; 2..16), or 0 (merged through the workspace) */
   size_t workspace_bytes;    /* tickets max(64 KiB, (B*Hkv+64)*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;
@@ -230,9 +213,7 @@ int decode_kv_append(const decode_attn_params* p, const void* k_new, const void*
  * position; sequences with seq_len 0 get no row) followed by decode_attn.
  * The CTA holding each sequence's last position writes the new rows of its
  * KV head before it streams its tiles.  Arguments as decode_attn plus k_new,
- * v_new ([B][Hkv][D] fp16 device); k_pages and v_pages are written.  On an
- * all-heads plan (DECODE_ATTN_SCHEDULE_ALL_HEADS) the append runs as its own
- * kernel just before the attention launch (two launches, same result).
+ * v_new ([B][Hkv][D] fp16 device); k_pages and v_pages are written.
  */
 int decode_attn_append(const decode_attn_params* p, const void* q, const void* k_new,
                        const void* v_new, void* k_pages, void* v_pages,

@@ -27,13 +27,11 @@ __all__ = [
     "DEV_BAD_LEN", "DEV_BAD_PAGE", "DEV_OVER_HINT", "DEV_TIMEOUT", "DEV_CHECK",
     "decode_attn_static_scratch", "decode_attn_workspace_clear", "DEV_WORKSPACE",
     "decode_kv_append", "decode_attn_append", "DTYPE_FP16", "DTYPE_BF16",
-    "SCHEDULE_AUTO", "SCHEDULE_GRID", "SCHEDULE_PERSISTENT", "SCHEDULE_CLUSTER",
-    "SCHEDULE_ALL_HEADS",
+    "SCHEDULE_AUTO", "SCHEDULE_GRID", "SCHEDULE_CLUSTER",
 ]
 
 VARIANT_AUTO, VARIANT_SIMT, VARIANT_MMA = 0, 1, 2
-SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_PERSISTENT, SCHEDULE_CLUSTER = 0, 1, 2, 3
-SCHEDULE_ALL_HEADS = 4
+SCHEDULE_AUTO, SCHEDULE_GRID, SCHEDULE_CLUSTER = 0, 1, 2
 DTYPE_FP16, DTYPE_BF16 = 0, 1
 DEV_BAD_LEN, DEV_BAD_PAGE, DEV_OVER_HINT, DEV_TIMEOUT, DEV_WORKSPACE = 1, 2, 4, 8, 16
 DEV_CHECK = 32  # the checked build only: an index outside its buffer
@@ -62,8 +60,8 @@ class DecodeAttnParams(ctypes.Structure):
 class DecodeAttnPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "split", "variant", "group_pad", "tile_tokens", "chunk_tokens", "max_shards",
-        "grid_x", "grid_y", "grid_z", "ctas_per_sm", "persistent", "head_fastest",
-        "ring_stages", "cluster", "all_heads")] + [
+        "grid_x", "grid_y", "grid_z", "ctas_per_sm", "head_fastest", "ring_stages",
+        "cluster")] + [
         ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
@@ -129,9 +127,8 @@ def make_params(q, k_pages, page_table, scale: float, window: int = 0,
     positions per sequence), k_pages [P,PS,Hkv,D], page_table [B,maxPages].
     ``max_seq_len`` is a host-side bound on seq_lens (it sizes the grid;
     None = the page table's capacity).  ``schedule``: SCHEDULE_AUTO (the
-    planner's grid or cluster plan), SCHEDULE_GRID, SCHEDULE_PERSISTENT,
-    SCHEDULE_CLUSTER or SCHEDULE_ALL_HEADS (the last three on request only;
-    a schedule the shape cannot take raises DecodeAttnError at planning)."""
+    planner's grid or cluster plan), SCHEDULE_GRID or SCHEDULE_CLUSTER (a
+    schedule the shape cannot take raises DecodeAttnError at planning)."""
     if len(q.shape) == 4:
         B, T, Hq, D = q.shape
     else:

@@ -21,10 +21,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMinChunk = 128;        // shortest shard the planner picks, tokens
 constexpr int kLargeChunkCap = 2048;  // longest shard for large work, unless span / 16
 constexpr int kSmemPerSm = 228 * 1024;
-constexpr int kMaxCluster = 8;  // portable thread-block cluster size
-constexpr int kAllHeadsKv = 8;            // KV heads of the all-heads kernel (its consumer warps)
-constexpr int64_t kAllHeadsMinChunk = 256;
-constexpr int64_t kAllHeadsMaxChunk = 1024;  // its per-item page-row table
+constexpr int kMaxCluster = 16;  // largest thread-block cluster (above 8: non-portable)
 // Cost model of a one-wave split plan, calibrated on GB300 chunk sweeps (one,
 // two and four sequences of 16 Ki..128 Ki tokens, the Llama-3.1-8B shape, the
 // windowed long case):
@@ -97,7 +94,7 @@ int check_params(const decode_attn_params* p) {
   if (!std::isfinite(p->scale) || p->num_queries > 4096) return DECODE_ATTN_ERR_SHAPE;
   if (p->dtype != DECODE_ATTN_DTYPE_FP16 && p->dtype != DECODE_ATTN_DTYPE_BF16)
     return DECODE_ATTN_ERR_SHAPE;
-  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_ALL_HEADS) return DECODE_ATTN_ERR_SHAPE;
+  if (p->schedule < 0 || p->schedule > DECODE_ATTN_SCHEDULE_CLUSTER) return DECODE_ATTN_ERR_SHAPE;
   return DECODE_ATTN_OK;
 }
 
@@ -106,7 +103,7 @@ int check_params(const decode_attn_params* p) {
 // has more groups: a zero-filled workspace therefore stays valid across calls
 // with different shapes, since every completed call leaves its tickets zero.
 constexpr size_t kTicketRegion = 64 * 1024;
-// Group tickets [B*Hkv], then the all-heads schedule's work counters.
+// Group tickets [B*Hkv] (and 64 spare words).
 size_t ticket_region_bytes(const decode_attn_params* p) {
   const size_t need = (((size_t)p->batch * p->num_kv_heads + 64) * 4 + 255) / 256 * 256;
   return need > kTicketRegion ? need : kTicketRegion;
@@ -129,13 +126,6 @@ size_t simt_smem_bytes(int head_dim) {
     case 64: return SimtCfg<64>::kSmemBytes;
     case 128: return SimtCfg<128>::kSmemBytes;
     default: return SimtCfg<256>::kSmemBytes;
-  }
-}
-int persist_smem(int head_dim, int nt8) {
-  switch (head_dim) {
-    case 64: return persist_smem_d64(nt8);
-    case 128: return persist_smem_d128(nt8);
-    default: return persist_smem_d256(nt8);
   }
 }
 // Shards per sequence for plans whose grid fits in one wave of CTA slots
@@ -264,49 +254,6 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   const int64_t max_shards = ceil_div(span, chunk);
   if (max_shards > 65535) return DECODE_ATTN_ERR_SHAPE;
 
-  // Persistent balanced schedule (one CTA per resident slot, equal tile
-  // ranges per KV head) only on request: on GB300 it measured level with the
-  // grid schedule on the batched mix (197.9 vs 197.7 us), behind it on the
-  // long context (317.9 vs 314.2 us) and well behind on a thousand short
-  // sequences (367 vs 217 us), where its per-segment fold and merge cost more
-  // than the grid's extra CTAs.
-  const int64_t units_all = (int64_t)p->batch * p->num_kv_heads;
-  const int64_t tiles_bound = units_all * ceil_div(span, kTile);
-  const bool persist_ok = variant == DECODE_ATTN_VARIANT_MMA && p->batch >= 1 &&
-                          p->batch <= kPersistMaxBatch && units_all <= 16384 &&
-                          tiles_bound < (int64_t(1) << 30) && p->num_kv_heads <= num_sms;
-  const bool large_work = units_all * span * 4 * p->head_dim > (int64_t)num_sms * ctas_per_sm *
-                                                                   (int64_t(1) << 20);
-  bool persistent = false;
-  if (p->schedule == DECODE_ATTN_SCHEDULE_PERSISTENT) {
-    if (!persist_ok) return DECODE_ATTN_ERR_VARIANT;
-    persistent = true;
-  }
-  (void)large_work;
-  if (persistent) {
-    // dynamic + static shared memory + the per-CTA reservation; the launch
-    // uses the device's own occupancy figure, never more CTAs than planned
-    const int per_cta = persist_smem(p->head_dim, group_pad / 8) + 7 * 1024 + 512;
-    const int cps = std::max(1, kSmemPerSm / per_cta);
-    const int64_t nc = (int64_t)num_sms * cps;
-    const size_t slots = (size_t)nc * 2 * T * G;
-    plan->variant = variant;
-    plan->group_pad = group_pad;
-    plan->tile_tokens = kTile;
-    plan->chunk_tokens = kTile;
-    plan->max_shards = 0;
-    plan->split = 1;
-    plan->persistent = 1;
-    plan->ring_stages = p->head_dim == 64 ? 6 : 3;
-    plan->grid_x = (int32_t)nc;
-    plan->grid_y = 1;
-    plan->grid_z = 1;
-    plan->ctas_per_sm = cps;
-    plan->workspace_bytes = ticket_region_bytes(p) + round_up(slots * sizeof(float2), 256) +
-                            round_up(slots * p->head_dim * 4, 256);
-    return DECODE_ATTN_OK;
-  }
-
   plan->variant = variant;
   plan->group_pad = group_pad;
   plan->tile_tokens = kTile;
@@ -340,13 +287,10 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   // Cluster merge: the shards of a (KV head, sequence) as one thread-block
   // cluster (grid x = shards), merged through distributed shared memory
   // instead of the workspace and a ticket, for one-wave tensor-core split
-  // plans of 2..8 shards (a portable cluster).  The planner takes it when the
-  // grid fills at least 4/5 of the CTA slots or the step is small: a cluster's
-  // CTAs are packed onto neighbouring SMs of one GPC, so a sparse grid of
-  // clusters leaves SMs idle.  GB300, against the workspace merge on the same
-  // plans: long case 305.4 -> 303.3 us, window 4096 23.2 -> 22.5 us, four
-  // 32768-token sequences 85.2 -> 84.2 us, the D = 64 sweep shape 14.9 ->
-  // 14.4 us; two 65536-token sequences at 8 shards (128 CTAs) 93.2 -> 104.5.
+  // plans of 2..16 shards.  The planner takes it when the grid fills at
+  // least 4/5 of the CTA slots or the step is small: a cluster's CTAs are
+  // packed onto neighbouring SMs of one GPC, so a sparse grid of clusters
+  // leaves SMs idle.
   const bool cluster_ok = variant == DECODE_ATTN_VARIANT_MMA && plan->split && !head_fastest &&
                           !shallow && max_shards >= 2 && max_shards <= kMaxCluster;
   const int64_t step_bytes =
@@ -357,49 +301,6 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   } else if (p->schedule == DECODE_ATTN_SCHEDULE_AUTO && cluster_ok &&
              (ctas * 5 >= slots_all * 4 || step_bytes <= (int64_t(32) << 20))) {
     plan->cluster = (int32_t)max_shards;
-  }
-  // All-heads schedule, on request: one persistent CTA per SM streams
-  // 16-position slices of all 8 KV heads per stage (whole page rows) instead
-  // of one head's rows per CTA.  A streaming probe without arithmetic read
-  // the batched workload's page-16 pool at 7.13 TB/s that way (6.25 with
-  // per-head 2 KB boxes), but the kernel itself measured behind the grid
-  // schedule on GB300 (batched 208 vs 193 us, a thousand short sequences 186
-  // vs 180 us): one CTA's eight consumer warps sustain about 49 GB/s, so the
-  // tail and the item boundaries cost more than the better reads gain.
-  const bool ah_ok = variant == DECODE_ATTN_VARIANT_MMA &&
-                     (p->head_dim == 64 || p->head_dim == 128) &&
-                     p->num_kv_heads == kAllHeadsKv && T == 1 && group_pad == 8 &&
-                     p->page_size >= 16 && p->batch >= 1;
-  int64_t ah_chunk = 0;
-  if (ah_ok) {
-    ah_chunk = force_chunk > 0
-                   ? round_up(force_chunk, kTile)
-                   : std::min<int64_t>(kAllHeadsMaxChunk,
-                                       std::max<int64_t>(kAllHeadsMinChunk,
-                                                         round_up(ceil_div(span, 16), kTile)));
-  }
-  bool all_heads = false;
-  if (p->schedule == DECODE_ATTN_SCHEDULE_ALL_HEADS) {
-    if (!ah_ok || ah_chunk > kAllHeadsMaxChunk) return DECODE_ATTN_ERR_VARIANT;
-    all_heads = true;
-  }
-  if (all_heads) {
-    const int64_t shards = ceil_div(span, ah_chunk);
-    if (shards > 65535 || (int64_t)p->batch * shards > (int64_t(1) << 30))
-      return DECODE_ATTN_ERR_SHAPE;
-    plan->split = 1;
-    plan->tile_tokens = 16;
-    plan->chunk_tokens = (int32_t)ah_chunk;
-    plan->max_shards = (int32_t)shards;
-    plan->grid_x = num_sms;
-    plan->grid_y = 1;
-    plan->grid_z = 1;
-    plan->ctas_per_sm = 1;
-    plan->persistent = 0;
-    plan->head_fastest = 0;
-    plan->cluster = 0;
-    plan->all_heads = 1;
-    plan->ring_stages = p->head_dim == 64 ? 6 : 3;
   }
   if (plan->split) {
     // shard tickets (a fixed region first), (m, l) pairs, fp32 accumulators
@@ -454,51 +355,15 @@ int encode_pool_map(CUtensorMap* map, const void* base, const decode_attn_params
 // of 16) went from 197.2 to 193-195 us with the whole piece in one box.
 // 64-row pieces keep one box per 64-dim chunk (8 KB each), which measured
 // faster there (one 131072-token sequence 89.1 against 90.2 us).
-int encode_pool_map_swizzled_boxes(CUtensorMap* map, const void* base,
-                                   const decode_attn_params* p, int box_t, bool per_chunk) {
-  auto fn = encode_fn();
-  if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
-  const int D = p->head_dim;
-  cuuint64_t dims[4] = {64, (cuuint64_t)p->num_pages * p->page_size,
-                        (cuuint64_t)p->num_kv_heads, (cuuint64_t)D / 64};
-  cuuint64_t strides[3] = {(cuuint64_t)p->num_kv_heads * D * 2, (cuuint64_t)D * 2, 128};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_t, 1,
-                       (box_t < kTile && !per_chunk) ? (cuuint32_t)D / 64 : 1u};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
-                                    ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = fn(map, et, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DECODE_ATTN_OK : DECODE_ATTN_ERR_TENSOR_MAP;
-}
-
 int encode_pool_map_swizzled(CUtensorMap* map, const void* base, const decode_attn_params* p,
                              int box_t) {
-  return encode_pool_map_swizzled_boxes(map, base, p, box_t, false);
-}
-
-// The persistent kernel's view: one box per (piece, 64-dim chunk), its
-// stages laid out [D/64][64 rows][64] as one piece.
-int encode_pool_map_chunks(CUtensorMap* map, const void* base, const decode_attn_params* p,
-                           int box_t) {
-  return encode_pool_map_swizzled_boxes(map, base, p, box_t, true);
-}
-
-// 4-D view (64 dims, P*PS token rows, kv head, D/64 chunks) with the 128-byte
-// swizzle, for the all-heads kernel: one box = 16 rows x all Hkv heads x 64
-// dims, written to shared memory as [head][16 rows][64 dims] (row t of head
-// h is 128-byte row 16h + t, its 16-byte chunk c at c ^ (t % 8)).
-int encode_pool_map_heads(CUtensorMap* map, const void* base, const decode_attn_params* p,
-                          int /*box_t*/) {
   auto fn = encode_fn();
   if (!fn) return DECODE_ATTN_ERR_TENSOR_MAP;
   const int D = p->head_dim;
   cuuint64_t dims[4] = {64, (cuuint64_t)p->num_pages * p->page_size,
                         (cuuint64_t)p->num_kv_heads, (cuuint64_t)D / 64};
   cuuint64_t strides[3] = {(cuuint64_t)p->num_kv_heads * D * 2, (cuuint64_t)D * 2, 128};
-  cuuint32_t box[4] = {64, 16, (cuuint32_t)p->num_kv_heads, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_t, 1, box_t < kTile ? (cuuint32_t)D / 64 : 1u};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType et = p->dtype == DECODE_ATTN_DTYPE_BF16
                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -539,11 +404,8 @@ int workspace_views(const decode_attn_params* p, const decode_attn_plan& plan, v
   if (!plan.split) return DECODE_ATTN_OK;
   if (!ws || ws_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(ws) & 255))
     return DECODE_ATTN_ERR_WORKSPACE;
-  const int G = p->num_q_heads / p->num_kv_heads;
-  const size_t rows = plan.persistent
-                          ? (size_t)plan.grid_x * 2 * num_queries(p) * G
-                          : (size_t)p->batch * num_queries(p) * p->num_q_heads *
-                                (size_t)plan.max_shards;
+  const size_t rows =
+      (size_t)p->batch * num_queries(p) * p->num_q_heads * (size_t)plan.max_shards;
   char* base = static_cast<char*>(ws);
   const size_t tickets = ticket_region_bytes(p);
   const size_t ml_bytes = round_up(rows * sizeof(float2), 256);
@@ -563,10 +425,8 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   if (p->batch == 0) return DECODE_ATTN_OK;
   SplitLaunch L{};
   const int box_t = std::min(p->page_size, kTile);
-  auto encode = plan.all_heads    ? encode_pool_map_heads
-                : plan.persistent ? encode_pool_map_chunks
-                : plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled
-                                                           : encode_pool_map;
+  auto encode =
+      plan.variant == DECODE_ATTN_VARIANT_MMA ? encode_pool_map_swizzled : encode_pool_map;
   int st = encode(&L.tmap_k, k_pages, p, box_t);
   if (!st) st = encode(&L.tmap_v, v_pages, p, box_t);
   if (st) return st;
@@ -598,6 +458,10 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.T = num_queries(p);
   a.head_fastest = plan.head_fastest;
   a.batch = p->batch;
+  {
+    const int64_t cap = (int64_t)p->max_pages_per_seq * p->page_size;
+    a.len_hint = (int32_t)(p->max_seq_len > 0 ? std::min<int64_t>(p->max_seq_len, cap) : cap);
+  }
   // Test hook (tensor-core kernel): DECODE_ATTN_TEST_STALL_TX=n makes the
   // first stage's barrier of every CTA expect n bytes more than the stage
   // brings, so its wait runs out (about 2 s) and the kernel must report
@@ -609,11 +473,9 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.group_pad = plan.group_pad;
   L.variant = plan.variant;
   L.dtype = p->dtype;
-  L.persistent = plan.persistent;
   L.cluster = plan.cluster;
-  L.all_heads = plan.all_heads;
-  L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && !plan.persistent && !plan.all_heads &&
-               p->head_dim <= 128 && plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
+  L.shallow = (plan.variant == DECODE_ATTN_VARIANT_MMA && p->head_dim <= 128 &&
+               plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
                   ? 1
                   : 0;  // the launcher has the shallow kernels the planner picks from
   L.batch = p->batch;
@@ -621,28 +483,6 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   L.stream = stream;
   // the shard tickets are zero on entry: the last CTA of each group clears
   // its own, so a workspace cleared once stays clear across calls
-  if (plan.all_heads && k_new != nullptr) {
-    // the all-heads kernel has no fused append: the step's rows go to their
-    // pages first (positions seq_lens[b] - 1), then the attention reads them
-    KvAppendArgs ka;
-    ka.k_new = static_cast<const uint4*>(k_new);
-    ka.v_new = static_cast<const uint4*>(v_new);
-    ka.positions = seq_lens;
-    ka.pos_offset = -1;
-    ka.page_table = page_table;
-    ka.k_pages = static_cast<uint4*>(const_cast<void*>(k_pages));
-    ka.v_pages = static_cast<uint4*>(const_cast<void*>(v_pages));
-    ka.err = err_flag;
-    ka.B = p->batch;
-    ka.Hkv = p->num_kv_heads;
-    ka.chunks = p->head_dim / 8;
-    ka.page_size = p->page_size;
-    ka.max_pages = p->max_pages_per_seq;
-    ka.num_pages = p->num_pages;
-    if ((st = cuda_status(launch_kv_append(ka, stream)))) return st;
-    a.k_new = nullptr;
-    a.v_new = nullptr;
-  }
   switch (p->head_dim) {
     case 64: return cuda_status(launch_split_d64(L));
     case 128: return cuda_status(launch_split_d128(L));
@@ -654,7 +494,6 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
                 const int32_t* seq_lens, void* out, const Workspace& ws, int32_t* err_flag,
                 cudaStream_t stream) {
   if (!plan.split || p->batch == 0) return DECODE_ATTN_OK;
-  if (plan.persistent) return DECODE_ATTN_OK;  // its merges ran inside the split launch
   CombineArgs a{};
   a.seq_lens = seq_lens;
   a.err = err_flag;

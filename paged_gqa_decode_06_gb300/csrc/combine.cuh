@@ -28,10 +28,9 @@ struct CombineArgs {
   int32_t B, Hq, G, T, capacity, window, chunk, max_shards;
 };
 
-// Bounds of the partial slots (the checked build; no bound for the
-// persistent schedule's own slots, max_shards = 0).
+// Bounds of the partial slots (the checked build).
 __device__ __forceinline__ size_t slot_bound(const CombineArgs& a) {
-  return a.max_shards > 0 ? (size_t)a.B * a.T * a.Hq * a.max_shards : ~size_t(0);
+  return (size_t)a.B * a.T * a.Hq * a.max_shards;
 }
 
 // Output row of the group's r-th query row (r = t * G + g): query t of
@@ -268,9 +267,9 @@ template <int D, class E>
 __global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
   extern __shared__ __align__(16) uint8_t merge_smem[];
   const int h = blockIdx.x, b = blockIdx.y;
+  grid_dependency_wait();  // the lengths and partials may come from the kernel before
   const SeqRange r =
       seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T);
-  grid_dependency_wait();
   merge_group<D, E>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
                     kShardBlock, [] { __syncthreads(); },
                     GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});

@@ -78,13 +78,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 4-D tiled TMA load (used with the 128-byte swizzled view of the pool).
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
+// An L2 cache policy that evicts the lines a load brings in first: every K/V
+// byte of a step is read exactly once.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 4-D tiled TMA load (the 128-byte swizzled view of the pool) into this
+// CTA's shared memory, completing on `bar`, with an L2 cache policy
+// (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, uint32_t bar,
+                                                 uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+      "l"(policy)
       : "memory");
 }
 

@@ -6,9 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "combine.cuh"
-#include "split_allheads.cuh"
 #include "split_mma.cuh"
-#include "split_persistent.cuh"
 #include "split_simt.cuh"
 
 namespace pgd {
@@ -21,18 +19,13 @@ struct SplitLaunch {
   int group_pad;
   int variant;
   int dtype;
-  int persistent;   // launch the persistent kernel (at most grid.x CTAs)
   int shallow;      // tensor-core kernel with the shallow ring (MmaCfg kShallow)
   int cluster;      // > 0: the cluster-merge kernel, clusters of this many CTAs along x
-  int all_heads;    // the all-heads kernel (grid.x CTAs, one per SM)
   int batch;
   int num_sms;
   cudaStream_t stream;
 };
 
-int persist_smem_d64(int nt8);
-int persist_smem_d128(int nt8);
-int persist_smem_d256(int nt8);
 cudaError_t launch_split_d64(const SplitLaunch& L);
 cudaError_t launch_split_d128(const SplitLaunch& L);
 cudaError_t launch_split_d256(const SplitLaunch& L);
@@ -52,9 +45,6 @@ struct KvAppendArgs {
   int32_t B, Hkv, chunks, page_size, max_pages, num_pages;
 };
 cudaError_t launch_kv_append(const KvAppendArgs& a, cudaStream_t stream);
-
-// Dynamic shared memory of the persistent kernel for (head_dim, row tiles).
-int persist_smem(int head_dim, int nt8);
 
 // Resident CTAs per SM the kernels are sized for (shared-memory bound).
 int simt_ctas_per_sm(int head_dim);

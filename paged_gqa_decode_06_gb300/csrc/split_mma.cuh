@@ -1,16 +1,21 @@
 // Split decode-attention kernel, tensor-core variant.
 //
-// Same CTA shape, shard arithmetic, TMA producer and fixed-order epilogue as
-// the CUDA-core variant (split_simt.cuh); only the q.k and p.v products move
-// to mma.sync.m16n8k16 (fp16 x fp16 -> fp32), with tokens on the 16-row M
-// side and the G query heads of the group on the N side (N = 8 per tile, two
-// tiles for G up to 16):
-//   scores^T [16 tok x 8 heads] = K [16 tok x D] . Q^T [D x 8 heads]
-//   out^T    [D x 8 heads]     += V^T [D x 16 tok] . P^T [16 tok x 8 heads]
-// The score accumulator's fragment is transposed into the P^T operand with
-// movmatrix; P is split into an fp16 head and an fp16 remainder (two mma per
-// tile) so the weights keep about twice the element format's bits (22 for
-// fp16, 16 for bf16).  Templated on the element format E (fp16 or bf16).
+// One CTA owns (shard s, KV head h, sequence b): a producer warp streams the
+// shard's K and V rows of head h through a shared-memory ring with TMA boxes,
+// and every K/V row read serves all G query heads of the group
+// (BackendStack21/mlx-runner pull request 3, commit "GQA-shared split
+// attention").  The products run on the tensor cores with mma.sync.m16n8k16
+// (16-bit inputs, fp32 accumulation), tokens on the 16-row M side and the
+// group's query rows on the N side (one n8 tile, or two for up to 16 rows):
+//   scores^T [16 tok x 8 rows] = K [16 tok x D] . Q^T [D x 8 rows]
+//   out^T    [D x 8 rows]     += V^T [D x 16 tok] . P^T [16 tok x 8 rows]
+// Each of the four consumer warps takes 16 positions of every 64-position
+// stage; a shard's partial (running max, sum, fp32 accumulator; apache/tvm
+// pull request 20426, sharded-nest commit) is the warps' states folded in
+// fixed order.
+// The score fragment is transposed into the P^T operand with movmatrix; P is
+// split into a 16-bit head and a 16-bit remainder (two mma per tile), so the
+// weights keep about 22 (fp16) / 16 (bf16) bits.
 //
 // A stage's K (and V) tile is 64 tokens made of pieces of box_t = min(page,
 // 64) rows, one TMA box each, every piece laid out [D/64][box_t rows][64
@@ -19,7 +24,7 @@
 // distinct bank groups (swz_offset).
 #pragma once
 
-#include "split_simt.cuh"  // SplitArgs, zero_group_rows
+#include "split_simt.cuh"  // SplitArgs, zero_group_rows, append_new_rows, merge_if_last
 
 namespace pgd {
 
@@ -28,13 +33,29 @@ namespace pgd {
 // round trips overlap.
 template <int D, bool kShallow = false>
 struct MmaCfg {
-  static constexpr int kWarps = 4;  // consumer warps, 16 tokens of each stage apiece
+  static constexpr int kWarps = 4;  // consumer warps, D / 4 output dims apiece
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kStages = (D == 64) ? (kShallow ? 4 : 6) : (kShallow ? 2 : 3);
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kRingBytes + 1024;
+};
+
+// Shared memory a cluster plan's CTA receives the group's partials in
+// (after the ring): for each of the S CTAs of the cluster, its values of
+// this CTA's slice of the (row, 4 dims) items, then its (m, l) per row.
+struct ClusterRecv {
+  int per;         // items of a slice: ceil(rows * D / 4 / S)
+  int acc_bytes;   // S * per float4
+  int bytes;       // + S * rows float2
+  __host__ __device__ static ClusterRecv of(int rows, int D, int S) {
+    ClusterRecv c;
+    c.per = (rows * (D / 4) + S - 1) / S;
+    c.acc_bytes = S * c.per * 16;
+    c.bytes = c.acc_bytes + S * rows * 8;
+    return c;
+  }
 };
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -70,29 +91,20 @@ __device__ __forceinline__ uint32_t swz_offset(int t, int d, int ps) {
                     ((((d >> 3) & 7) ^ (t & 7)) << 4));
 }
 
-struct NoRelease {
-  __device__ void operator()() const {}
-};
-
 // One consumer warp's 16 positions [tok0, tok0 + 16) of a staged tile:
 // scores^T = K . Q^T, the per-column causal / window mask, the online
-// softmax update and out^T += V^T . P^T.  kt points at the stage's K tile of
-// kRows rows in pieces of 2^ps rows (swz_offset), the warp's 16 rows at
-// 16 * warp (V follows at kRows * D * 2 bytes); [lo, hi) is the union of the
-// columns' ranges clipped to the shard, and the block must overlap it.  kFetchFirst: all of
-// the warp's K and V fragments are loaded into registers first and
-// release() is called before any arithmetic, so the stage can be refilled
-// while the warp computes (the same operations in the same order).
-template <int D, int NT8, class E, int kRows = kTile, bool kFetchFirst = false,
-          class Release = NoRelease>
+// softmax update and out^T += V^T . P^T.  kt points at the stage's K tile in
+// pieces of 2^ps rows (swz_offset), the warp's 16 rows at 16 * warp (V
+// follows at kTile * D * 2 bytes); [lo, hi) is the union of the columns'
+// ranges clipped to the shard, and the block must overlap it.
+template <int D, int NT8, class E>
 __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int tok0, int lo,
                                           int hi, const int (&col_lo)[NT8][2],
                                           const int (&col_hi)[NT8][2],
                                           const uint32_t (&qf)[NT8][D / 16][2], float scale_log2,
                                           float (&acc)[D / 16][NT8][4], float (&m_run)[NT8][2],
-                                          float (&l_part)[NT8][2], int ps,
-                                          Release release = {}) {
-  constexpr int kTileBytes = kRows * D * 2;
+                                          float (&l_part)[NT8][2], int ps) {
+  constexpr int kTileBytes = kTile * D * 2;
   constexpr int KS = D / 16;
   const int gid = lane >> 2;
   const int mat = lane >> 3, mrow = lane & 7;
@@ -116,47 +128,16 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
     fence_proxy_async_smem();
     __syncwarp();
   }
-  constexpr int kHeld = kFetchFirst ? KS : 1;
-  uint32_t kf[kHeld][4], vf[kHeld][4];
-  if constexpr (kFetchFirst) {
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
-      ldmatrix_x4(kf[ks], kbase + swz_offset<D>(k_tok, ks * 16 + k_dof, ps));
-#pragma unroll
-    for (int mi = 0; mi < KS; ++mi)
-      ldmatrix_x4_trans(vf[mi], vbase + swz_offset<D>(v_tok, mi * 16 + v_dof, ps));
-    release();
-  }
   // scores^T = K . Q^T
   float sc[NT8][4];
 #pragma unroll
   for (int j = 0; j < NT8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-  if constexpr (kFetchFirst) {
-    // two independent accumulation chains (even and odd k-steps), added at
-    // the end: half the dependent mma latency on the warp's critical path
-    float sc1[NT8][4];
 #pragma unroll
-    for (int j = 0; j < NT8; ++j) sc1[j][0] = sc1[j][1] = sc1[j][2] = sc1[j][3] = 0.f;
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t af[4];
+    ldmatrix_x4(af, kbase + swz_offset<D>(k_tok, ks * 16 + k_dof, ps));
 #pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-#pragma unroll
-      for (int j = 0; j < NT8; ++j) {
-        ElemOps<E>::mma(sc[j], kf[ks], qf[j][ks][0], qf[j][ks][1]);
-        ElemOps<E>::mma(sc1[j], kf[ks + 1], qf[j][ks + 1][0], qf[j][ks + 1][1]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NT8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[j][e] += sc1[j][e];
-  } else {
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t af[4];
-      ldmatrix_x4(af, kbase + swz_offset<D>(k_tok, ks * 16 + k_dof, ps));
-#pragma unroll
-      for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
-    }
+    for (int j = 0; j < NT8; ++j) ElemOps<E>::mma(sc[j], af, qf[j][ks][0], qf[j][ks][1]);
   }
   // online softmax over this block's 16 positions
   const int tok_a = tok0 + gid, tok_b = tok0 + gid + 8;
@@ -213,11 +194,7 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
 #pragma unroll
   for (int mi = 0; mi < KS; ++mi) {
     uint32_t af[4];
-    if constexpr (kFetchFirst) {
-      af[0] = vf[mi][0], af[1] = vf[mi][1], af[2] = vf[mi][2], af[3] = vf[mi][3];
-    } else {
-      ldmatrix_x4_trans(af, vbase + swz_offset<D>(v_tok, mi * 16 + v_dof, ps));
-    }
+    ldmatrix_x4_trans(af, vbase + swz_offset<D>(v_tok, mi * 16 + v_dof, ps));
 #pragma unroll
     for (int j = 0; j < NT8; ++j) {
       ElemOps<E>::mma(acc[mi][j], af, pb_hi[j][0], pb_hi[j][1]);
@@ -226,79 +203,261 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
   }
 }
 
-// Where a CTA of a cluster plan keeps its shard's partial for the cluster's
-// merge: after the warps' states in the (by then idle) ring, out [GP][D]
-// fp32, then (m, l) [GP] float2 (l = -1: a dead shard).
-template <int D, int NT8>
-struct ClusterPartial {
-  static constexpr int kRowStride = D + 4;
-  static constexpr int kOutOffset = ((MmaCfg<D>::kWarps * 8 * NT8 * kRowStride * 4) + 15) & ~15;
-  static constexpr int kMlOffset = kOutOffset + 8 * NT8 * D * 4;
-  static constexpr int kEnd = kMlOffset + 8 * NT8 * 8;
-  static_assert(kEnd <= MmaCfg<D>::kRingBytes, "the partial fits in the ring");
-};
-
 __device__ __forceinline__ uint8_t* ring_base() {
   extern __shared__ uint8_t smem_raw[];
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                     ~uintptr_t(1023));
 }
 
-// The split kernel's body, shared by the kernels below.  CL: a cluster plan
-// (one cluster per (KV head, sequence), one CTA per shard): the CTA leaves
-// its partial in its shared memory (and in the workspace, for
-// decode_attn_combine) and the kernel's cluster merge follows.
+// %cluster_ctarank / %cluster_nctarank, the split cluster barrier (arrive
+// right after the receive barrier's initialisation, wait only before the
+// first access to another CTA's shared memory), stores to another CTA's
+// shared memory and the remote release-arrive on its mbarrier.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded like mbar_wait (about two seconds), with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+
+// The cluster merge of a cluster plan (the S shards of one (KV head,
+// sequence) form one thread-block cluster; cluster rank = shard index).
+// Every CTA owns a slice of the group's (row, 4 dims) items: item
+// e = row * D / 4 + quad belongs to CTA e / per.  Each CTA pushes its folded
+// value of every item (cluster_push) and its (m, l) of every row
+// (cluster_push_ml) into the owners' receive buffers in distributed shared
+// memory; cluster_finish then has thread 0 arrive on every owner's receive
+// barrier with release semantics, waits (bounded, acquire) for this CTA's S
+// arrivals and merges its slice in ascending shard order with the workspace
+// merge's arithmetic (max, then c_s = 2^(m_s - M) with fused multiply-adds),
+// so both merges give the same bits.  Nothing is read from another CTA's
+// shared memory, so no CTA waits for another to finish reading before it
+// exits.  The receive buffer sits after the ring, so a CTA still streaming
+// can already receive.
+struct ClusterXchg {
+  uint32_t recv_acc, recv_ml;  // this CTA's receive buffer (shared::cta addresses)
+  int S, rank, R;
+  ClusterRecv cr;
+  __device__ ClusterXchg() {}
+  __device__ ClusterXchg(uint8_t* recv, int rows, int D) {
+    S = (int)cluster_size();
+    rank = (int)cluster_rank();
+    R = rows;
+    cr = ClusterRecv::of(rows, D, S);
+    recv_acc = smem_u32(recv);
+    recv_ml = recv_acc + cr.acc_bytes;
+  }
+  __device__ void push(int e, float4 v) const {
+    const int o = e / cr.per;
+    const uint32_t at = recv_acc + (uint32_t)((rank * cr.per + (e - o * cr.per)) * 16);
+    st_dsmem_f4(dsmem_addr(at, (uint32_t)o), v);
+  }
+  __device__ void push_ml(int r, float2 v) const {
+    const uint32_t at = recv_ml + (uint32_t)((rank * R + r) * 8);
+    for (int o = 0; o < S; ++o) st_dsmem_f2(dsmem_addr(at, (uint32_t)o), v);
+  }
+};
+
+template <int D, class E>
+__device__ __forceinline__ void cluster_finish(const SplitArgs& a, const ClusterXchg& x, int b,
+                                               int h, uint32_t recv_bar, uint8_t* recv,
+                                               int nthreads) {
+  named_barrier_sync(1, nthreads);  // every consumer's stores are issued
+  if (threadIdx.x == 0)
+    for (int o = 0; o < x.S; ++o) mbar_arrive_remote_release(dsmem_addr(recv_bar, (uint32_t)o));
+  // this CTA's slice: wait for the S partials, merge in shard order
+  __shared__ int recv_ok_s;
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait_cluster(recv_bar, 0);
+    if (!ok) raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
+    recv_ok_s = ok ? 1 : 0;
+  }
+  named_barrier_sync(1, nthreads);
+  // (every thread acquires as well; the phase is complete, so this returns)
+  if (recv_ok_s) mbar_wait_cluster(recv_bar, 0);
+  const int R = x.R, S = x.S, per = x.cr.per;
+  const float4* racc = reinterpret_cast<const float4*>(recv);
+  const float2* rml = reinterpret_cast<const float2*>(recv + x.cr.acc_bytes);
+  const int total = R * (D / 4);
+  const int e_end = min(total, (x.rank + 1) * per);
+  for (int e = x.rank * per + (int)threadIdx.x; e < e_end; e += nthreads) {
+    const int r = e / (D / 4), quad = e % (D / 4);
+    const int slot = e - x.rank * per;
+    float M = -INFINITY;
+    bool z = !recv_ok_s;
+    for (int j = 0; j < S; ++j) {
+      const float2 v = rml[j * R + r];
+      z |= v.y < 0.f;  // a shard saw a bad page or gave up waiting
+      M = fmaxf(M, v.x);
+    }
+    z |= M == -INFINITY;  // no shard holds a position of this row
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; !z && j < S; ++j) {
+      const float2 v = rml[j * R + r];
+      const float4 xv = racc[j * per + slot];
+      const float c = fast_exp2(v.x - M);
+      L = __fmaf_rn(c, v.y, L);
+      o.x = __fmaf_rn(c, xv.x, o.x);
+      o.y = __fmaf_rn(c, xv.y, o.y);
+      o.z = __fmaf_rn(c, xv.z, o.z);
+      o.w = __fmaf_rn(c, xv.w, o.w);
+    }
+    z |= L == 0.f;
+    const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
+    const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
+    const size_t row = group_row(b, h, r, a.T, a.G, a.Hq);
+    if (PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err))
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + row * D + 4 * quad) =
+          make_uint2(lo, hi);
+  }
+}
+
+// The split kernel's body.  SH: the shallow ring.  CL: a cluster plan (one
+// cluster per (KV head, sequence), one CTA per shard, cluster rank = shard),
+// merged through distributed shared memory (ClusterXchg, cluster_finish);
+// other split plans write their partial to the workspace and the group's last
+// CTA merges (merge_if_last).
 template <int D, int NT8, class E, bool SH, bool CL = false>
 __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
                                                const CUtensorMap& tmap_v, const SplitArgs& a) {
   using C = MmaCfg<D, SH>;
-  constexpr int GP = 8 * NT8;  // padded heads of the group
-  constexpr int KS = D / 16;   // k-steps of q.k, m-tiles of p.v
+  constexpr int KS = D / 16;  // k-steps of q.k
   constexpr int kWarps = C::kWarps;
+  constexpr int GP = 8 * NT8;  // padded query rows of the group
 
-  extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ __align__(8) uint64_t recv_bar;
   __shared__ int32_t coord_s[kMaxPieces];
   __shared__ float2 ml_s[kWarps][GP];
   __shared__ float cw_s[kWarps][GP];  // each warp's weight per row
   __shared__ float2 row_s[GP];        // (M, L) per row
   __shared__ int32_t bad_s;
   __shared__ volatile int32_t abort_s;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = ring_base();
 
-  // launched as a programmatic dependent of the preceding kernel: its CTAs
-  // may become resident while that kernel drains, but nothing is read or
-  // written before it has completed
+  // Before the dependency wait (nothing here touches global memory): the
+  // pipeline's barriers, the tensor maps' prefetch and, for a cluster plan,
+  // the receive barrier and this CTA's arrival at the cluster barrier that
+  // the exchange waits on.
+  if (threadIdx.x == kWarps * 32) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(smem_u32(&full_bar[st]), 1);
+      mbar_init(smem_u32(&empty_bar[st]), kWarps);
+    }
+    if constexpr (CL) mbar_init(smem_u32(&recv_bar), cluster_size());
+    fence_mbar_init();
+    abort_s = 0;
+    bad_s = 0;
+  }
+  __syncthreads();
+  if constexpr (CL) cluster_arrive_relaxed();
+  // launched as a programmatic dependent of the preceding kernel: nothing is
+  // read or written before that kernel has completed
   grid_dependency_wait();
-  // a kernel launched after this one (a combine, the next step) may be
-  // scheduled now; it waits the same way before touching memory
+  // a kernel launched after this one (the next step) may be scheduled now;
+  // it waits the same way before touching memory
   grid_launch_dependents();
   // grid order: head fastest for plans of several waves (the Hkv CTAs of one
   // (sequence, shard) start together and read the rows of the same positions,
   // adjacent in the pool, side by side), shard fastest for one-wave plans
-  // (a group's shards run on neighbouring SMs for its merge)
+  // (a group's shards run on neighbouring SMs, a cluster plan's in one
+  // cluster)
   const int h = a.head_fastest ? blockIdx.x : blockIdx.y;
   const int s = a.head_fastest ? blockIdx.y : blockIdx.x;
   const int b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
-                               a.max_shards, a.T);
+  const int capacity = a.max_pages * a.page_size;
+  const int box_t = a.box_tokens;
+  // The producer reads the page ids of the shard's first 32 pieces together
+  // with the length, under the guess that the sequence is as long as the
+  // plan's bound: a shard's first position depends on the length only
+  // through a window's start, so without a window the guess always holds
+  // (with one, when the sequence is that long); otherwise they are read again.
+  int spec_lo = -1, spec_phys = -1;
+  if (warp == kWarps) {
+    const SeqRange g =
+        seq_range(a.len_hint, a.window, capacity, a.chunk, a.max_shards, a.T);
+    if (g.status == 0 && s < g.nshards) {
+      spec_lo = g.base + s * a.chunk;
+      const int ptok = spec_lo + lane * box_t;
+      const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
+      if (ptok < capacity && PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err))
+        spec_phys = a.page_table[pi];
+    }
+  }
+  const SeqRange r = seq_range(a.seq_lens[b], a.window, capacity, a.chunk, a.max_shards, a.T);
+  const int R = a.T * a.G;  // query rows of the group: r = t * G + g
+  const int gid = lane >> 2, tig = lane & 3;
+
   if (r.status != 0 || s >= r.nshards) {
+    if (s == 0 && r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
     if constexpr (CL) {
-      // an empty partial (no position of any row); the cluster merge zeroes
-      // rows that no shard holds
-      if (s == 0 && r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
-      using P = ClusterPartial<D, NT8>;
-      uint8_t* base = ring_base();
-      float* po = reinterpret_cast<float*>(base + P::kOutOffset);
-      float2* pml = reinterpret_cast<float2*>(base + P::kMlOffset);
-      for (int e = threadIdx.x; e < GP * D; e += blockDim.x) po[e] = 0.f;
-      for (int g = threadIdx.x; g < GP; g += blockDim.x) pml[g] = make_float2(-INFINITY, 0.f);
-    } else {
-      if (s == 0) {
-        if (r.status != 0 && threadIdx.x == 0) raise_error(a.err, r.status);
-        zero_group_rows<D, GP>(a, b, h);
+      // an empty partial (no position of any row) still takes part in the
+      // cluster's exchange; the merge zeroes rows that no shard holds
+      if (warp < kWarps) {
+        uint8_t* recv = ring + C::kRingBytes;
+        const ClusterXchg x(recv, R, D);
+        cluster_wait();  // every CTA of the cluster has initialised its barriers
+        for (int e = threadIdx.x; e < R * (D / 4); e += kWarps * 32)
+          x.push(e, make_float4(0.f, 0.f, 0.f, 0.f));
+        for (int g = threadIdx.x; g < R; g += kWarps * 32)
+          x.push_ml(g, make_float2(-INFINITY, 0.f));
+        cluster_finish<D, E>(a, x, b, h, smem_u32(&recv_bar), recv, kWarps * 32);
       }
+    } else if (s == 0) {
+      zero_group_rows<D, 8 * NT8>(a, b, h);
     }
     return;
   }
@@ -307,145 +466,157 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   const int lo = max(r.start, shard_lo);
   const int hi = min(r.end, shard_lo + a.chunk);
   const int n_tiles = (hi - shard_lo + kTile - 1) / kTile;
-  const int box_t = a.box_tokens;
   const int pieces_per_tile = kTile / box_t;
   const int n_pieces = n_tiles * pieces_per_tile;
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
 
+  // Producer: the boxes of a stage are issued by several lanes at once
+  // (lane j its j-th box) after lane 0 has armed the stage's full barrier
+  // with its bytes; every box is read once, so it enters L2 with the
+  // evict-first policy.  The first stages go out before the block-wide
+  // barrier below, the rest after each stage is released.
+  const uint32_t box_bytes = box_t * D * 2;  // one piece: box_t rows, all D dims
+  const int per_piece = box_t < kTile ? 1 : D / 64;
+  const int nbox = pieces_per_tile * per_piece * 2;
+  const int pool_rows = a.num_pages * a.page_size;
+  auto issue_stage = [&](int i, uint64_t policy) {
+    const int st = i % C::kStages;
+    if (lane == 0)
+      // (stall_tx, a test's hook, is 0: the barrier expects the stage's bytes)
+      mbar_arrive_expect_tx(smem_u32(&full_bar[st]), C::kStageBytes + (i == 0 ? a.stall_tx : 0));
+    __syncwarp();
+    const uint32_t fb = smem_u32(&full_bar[st]);
+    const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
+    const uint32_t vdst = kdst + C::kTileBytes;
+    for (int jb = lane; jb < nbox; jb += 32) {
+      const int is_v = jb & 1;
+      const int pc = (jb >> 1) / per_piece, dc = (jb >> 1) % per_piece;
+      int coord = coord_s[i * pieces_per_tile + pc];
+      // (checked build) a box must lie inside the pool or start at its end,
+      // where TMA fills zeros
+      if (!PGD_IN(coord == pool_rows ? 0 : (int64_t)coord + box_t - 1, pool_rows, a.err))
+        coord = pool_rows;
+      const CUtensorMap* map = is_v ? &tmap_v : &tmap_k;
+      const uint32_t dst = is_v ? vdst : kdst;
+      if (box_t < kTile)  // one box holds the piece's D dims
+        tma_load_4d_hint(dst + pc * box_bytes, map, 0, coord, h, 0, fb, policy);
+      else  // 64-row pieces: one box per 64-dim chunk
+        tma_load_4d_hint(dst + dc * (kTile * 128), map, 0, coord, h, dc, fb, policy);
+    }
+  };
+  bool bad = false;
   if (warp == kWarps) {
-    int bad = 0;
-    const int oob = a.num_pages * a.page_size;  // past the pool: TMA writes zeros
+    // physical coordinates of every box of the shard
+    int any_bad = 0;
+    const int oob = pool_rows;  // past the pool: TMA writes zeros
+#pragma unroll 4
     for (int i = lane; i < n_pieces; i += 32) {
       const int ptok = shard_lo + i * box_t;
       int coord = oob;
       if (ptok < hi && ptok + box_t > lo) {
-        const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
-        const int phys =
-            PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err) ? a.page_table[pi] : -1;
+        int phys;
+        if (i == lane && shard_lo == spec_lo) {
+          phys = spec_phys;
+        } else {
+          const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
+          phys = PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err) ? a.page_table[pi] : -1;
+        }
         if (phys < 0 || phys >= a.num_pages) {
-          bad = 1;
+          any_bad = 1;
         } else {
           coord = phys * a.page_size + (ptok & (a.page_size - 1));
         }
       }
       coord_s[i] = coord;
     }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      bad_s = bad;
-      abort_s = 0;
-      for (int st = 0; st < C::kStages; ++st) {
-        mbar_init(smem_u32(&full_bar[st]), 1);
-        mbar_init(smem_u32(&empty_bar[st]), kWarps);
-      }
-      fence_mbar_init();
-      if (bad) raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
+    bad = __any_sync(0xffffffffu, any_bad) != 0;
+    if (lane == 0 && bad) {
+      bad_s = 1;
+      raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
+    }
+    if (!bad) {
+      if (a.k_new != nullptr && r.end - a.T < shard_lo + a.chunk && r.end > shard_lo)
+        append_new_rows<D>(a, r, b, h, shard_lo, lane);
+      const uint64_t policy = l2_evict_first_policy();
+      for (int i = 0; i < min(n_tiles, C::kStages); ++i) issue_stage(i, policy);
     }
   }
-  __syncthreads();
-  const bool bad = bad_s != 0;
+
+  // ------------------------------------------------ consumers' set-up
+  // Q^T operand fragments, held for the whole shard (loaded while the
+  // producer reads the page ids)
+  uint32_t qf[NT8][KS][2];
+  float acc[KS][NT8][4];
+  int col_lo[NT8][2], col_hi[NT8][2];
+  float m_run[NT8][2], l_part[NT8][2];
+  if (warp < kWarps) {
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) {
+      const int rr = 8 * j + gid;
+      size_t qr = group_row(b, h, rr < R ? rr : 0, a.T, a.G, a.Hq);
+      if (!PGD_IN(qr, (size_t)a.batch * a.T * a.Hq, a.err)) qr = 0;
+      const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + qr * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        if (rr < R) {
+          qf[j][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
+          qf[j][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig);
+        } else {
+          qf[j][ks][0] = qf[j][ks][1] = 0u;
+        }
+      }
+    }
+    // attended range of each of this lane's score columns (query rows
+    // 8j + 2*tig + e): causal up to the row's own position, window from there
+#pragma unroll
+    for (int j = 0; j < NT8; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int rr = 8 * j + 2 * tig + e;
+        const int t = rr < R ? rr / a.G : a.T - 1;
+        col_hi[j][e] = r.end - a.T + t + 1;
+        col_lo[j][e] = a.window > 0 ? max(0, col_hi[j][e] - a.window) : 0;
+        m_run[j][e] = -INFINITY;
+        l_part[j][e] = 0.f;
+      }
+#pragma unroll
+    for (int mi = 0; mi < KS; ++mi)
+#pragma unroll
+      for (int j = 0; j < NT8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
+  }
+  __syncthreads();  // the page ids and the bad-page flag are in shared memory
+  bad = bad_s != 0;
 
   if (warp == kWarps) {
-    if (a.k_new != nullptr && !bad) {
-      const int shard_lo_w = r.base + s * a.chunk;
-      if (r.end - a.T < shard_lo_w + a.chunk && r.end > shard_lo_w)
-        append_new_rows<D>(a, r, b, h, shard_lo_w, lane);
-    }
-    if (lane == 0 && !bad) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-      const uint32_t box_bytes = box_t * D * 2;  // one piece: box_t rows, all D dims
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+    if (!bad) {
+      const uint64_t policy = l2_evict_first_policy();
+      int issued = min(n_tiles, C::kStages);
+      for (int i = C::kStages; i < n_tiles; ++i) {
         const int st = i % C::kStages;
-        if (i >= C::kStages &&
-            !mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) & 1) ^ 1)) {
-          abort_s = 1;
-          raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
-          break;
-        }
-        if (abort_s) break;
-        const uint32_t fb = smem_u32(&full_bar[st]);
-        // (stall_tx, a test's hook, is 0: the barrier expects the stage's bytes)
-        mbar_arrive_expect_tx(fb, C::kStageBytes + (i == 0 ? a.stall_tx : 0));
-        const uint32_t kdst = smem_u32(ring + st * C::kStageBytes);
-        const uint32_t vdst = kdst + C::kTileBytes;
-        for (int pc = 0; pc < pieces_per_tile; ++pc) {
-          int coord = coord_s[i * pieces_per_tile + pc];
-          // (checked build) a box must lie inside the pool or start at its
-          // end, where TMA fills zeros
-          const int pool_rows = a.num_pages * a.page_size;
-          if (!PGD_IN(coord == pool_rows ? 0 : (int64_t)coord + box_t - 1, pool_rows, a.err))
-            coord = pool_rows;
-          if (box_t < kTile) {  // one box holds the piece's D dims
-            tma_load_4d(kdst + pc * box_bytes, &tmap_k, 0, coord, h, 0, fb);
-            tma_load_4d(vdst + pc * box_bytes, &tmap_v, 0, coord, h, 0, fb);
-          } else {  // 64-row pieces: one box per 64-dim chunk
-#pragma unroll
-            for (int dc = 0; dc < D / 64; ++dc) {
-              tma_load_4d(kdst + dc * (kTile * 128), &tmap_k, 0, coord, h, dc, fb);
-              tma_load_4d(vdst + dc * (kTile * 128), &tmap_v, 0, coord, h, dc, fb);
-            }
+        int go = 1;
+        if (lane == 0) {
+          if (!mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) & 1) ^ 1)) {
+            abort_s = 1;
+            raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
+            go = 0;
           }
+          if (abort_s) go = 0;
         }
+        if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        issue_stage(i, policy);
         issued = i + 1;
       }
-      for (int i = max(0, issued - C::kStages); i < issued; ++i)
-        mbar_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
+      // drain this CTA's copies in flight before the warp exits
+      if (lane == 0)
+        for (int i = max(0, issued - C::kStages); i < issued; ++i)
+          mbar_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
     }
     return;
   }
 
   // ------------------------------------------------------------ consumers
-  const int G = a.G;
-  const int gid = lane >> 2, tig = lane & 3;
   const int piece_shift = __ffs(box_t) - 1;  // a stage is pieces of box_t rows
-  // Q^T operand fragments, held for the whole shard
-  const int R = a.T * G;  // query rows of the group: r = t * G + g
-  uint32_t qf[NT8][KS][2];
-#pragma unroll
-  for (int j = 0; j < NT8; ++j) {
-    const int rr = 8 * j + gid;
-    size_t qr = group_row(b, h, rr < R ? rr : 0, a.T, G, a.Hq);
-    if (!PGD_IN(qr, (size_t)a.batch * a.T * a.Hq, a.err)) qr = 0;
-    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + qr * D;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      if (rr < R) {
-        qf[j][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig);
-        qf[j][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig);
-      } else {
-        qf[j][ks][0] = qf[j][ks][1] = 0u;
-      }
-    }
-  }
-  float acc[KS][NT8][4];
-#pragma unroll
-  for (int mi = 0; mi < KS; ++mi)
-#pragma unroll
-    for (int j = 0; j < NT8; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
-  // attended range of each of this lane's score columns (query rows
-  // 8j + 2*tig + e): causal up to the row's own position, window from there
-  int col_lo[NT8][2], col_hi[NT8][2];
-#pragma unroll
-  for (int j = 0; j < NT8; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int rr = 8 * j + 2 * tig + e;
-      const int t = rr < R ? rr / G : a.T - 1;
-      col_hi[j][e] = r.end - a.T + t + 1;
-      col_lo[j][e] = a.window > 0 ? max(0, col_hi[j][e] - a.window) : 0;
-    }
-  float m_run[NT8][2], l_part[NT8][2];
-#pragma unroll
-  for (int j = 0; j < NT8; ++j) {
-    m_run[j][0] = m_run[j][1] = -INFINITY;
-    l_part[j][0] = l_part[j][1] = 0.f;
-  }
-
   for (int i = 0; i < n_tiles && !bad; ++i) {
     const int st = i % C::kStages;
     if (!mbar_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1)) {
@@ -462,7 +633,7 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     if (lane == 0) mbar_arrive(smem_u32(&empty_bar[st]));
   }
 
-  // ---- merge the consumer warps in fixed order (deterministic) ----------
+  // ---- fold the consumer warps in fixed order (deterministic) -----------
 #pragma unroll
   for (int j = 0; j < NT8; ++j)
 #pragma unroll
@@ -518,7 +689,12 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   }
   named_barrier_sync(1, kWarps * 32);
   const bool dead = bad || abort_s != 0;
-
+  uint8_t* recv = ring + C::kRingBytes;  // a cluster plan's receive buffer
+  ClusterXchg x;
+  if constexpr (CL) {
+    x = ClusterXchg(recv, R, D);
+    cluster_wait();  // every CTA of the cluster has initialised its barriers
+  }
   // fold the warps, 4 dims per thread and pass, in warp order
   constexpr int kQuads = D / 4;
   for (int e = threadIdx.x; e < R * kQuads; e += kWarps * 32) {
@@ -529,16 +705,16 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     for (int w = 0; w < kWarps; ++w) {
       const float c = cw_s[w][g];
       if (c == 0.f) continue;
-      const float4 x =
+      const float4 v =
           *reinterpret_cast<const float4*>(acc_s + (w * GP + g) * kRowStride + 4 * q);
-      O.x += c * x.x;
-      O.y += c * x.y;
-      O.z += c * x.z;
-      O.w += c * x.w;
+      O.x += c * v.x;
+      O.y += c * v.y;
+      O.z += c * v.z;
+      O.w += c * v.w;
     }
-    const size_t row = group_row(b, h, g, a.T, G, a.Hq);
-    if (!PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err)) continue;
+    const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
     if (!a.split) {
+      if (!PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err)) continue;
       const bool z = dead || ML.y == 0.f;
       const uint32_t lo = (uint32_t)ElemOps<E>::round(z ? 0.f : O.x / ML.y) |
                           ((uint32_t)ElemOps<E>::round(z ? 0.f : O.y / ML.y) << 16);
@@ -546,123 +722,33 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
                           ((uint32_t)ElemOps<E>::round(z ? 0.f : O.w / ML.y) << 16);
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + row * D + 4 * q) =
           make_uint2(lo, hi);
-    } else {
-      const float4 Ow = dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
-      const float2 MLw = make_float2(ML.x, dead ? -1.f : ML.y);
-      if constexpr (CL) {
-        using P = ClusterPartial<D, NT8>;
-        *reinterpret_cast<float4*>(ring + P::kOutOffset + (g * D + 4 * q) * 4) = Ow;
-        if (q == 0) reinterpret_cast<float2*>(ring + P::kMlOffset)[g] = MLw;
-      }
-      const size_t slot = row * a.max_shards + s;
-      if (!PGD_IN(slot, (size_t)a.batch * a.T * a.Hq * a.max_shards, a.err)) continue;
-      *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) = Ow;
-      if (q == 0) a.ws_ml[slot] = MLw;
+      continue;
     }
+    // split: this shard's partial (m, l, acc) to the workspace slots (read by
+    // the group's merge, or later by decode_attn_combine; l = -1 marks a dead
+    // shard) and, for a cluster plan, to the item's owner in the cluster
+    const float4 Ow = dead ? make_float4(0.f, 0.f, 0.f, 0.f) : O;
+    const float2 MLw = make_float2(ML.x, dead ? -1.f : ML.y);
+    if constexpr (CL) {
+      x.push(e, Ow);
+      if (q == 0) x.push_ml(g, MLw);
+    }
+    const size_t slot = row * a.max_shards + s;
+    if (!PGD_IN(slot, (size_t)a.batch * a.T * a.Hq * a.max_shards, a.err)) continue;
+    *reinterpret_cast<float4*>(a.ws_acc + slot * D + 4 * q) = Ow;
+    if (q == 0) a.ws_ml[slot] = MLw;
   }
-  if constexpr (!CL) {
-    if (a.split) merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
+  if (!a.split) return;
+  if constexpr (CL) {
+    cluster_finish<D, E>(a, x, b, h, smem_u32(&recv_bar), recv, kWarps * 32);
+  } else {
+    merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
   }
-}
-
-// %cluster_ctarank / %cluster_nctarank, the cluster-wide barrier (every
-// thread of every CTA of the cluster; the release / acquire pair orders the
-// partials written before it with the reads after it) and loads from another
-// CTA's shared memory.
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return n;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(smem_u32(local)), "r"(rank));
-  return remote;
-}
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-// The cluster merge: every thread of the cluster's CTAs arrives here once the
-// body has returned (on any path); after the barrier each CTA merges its
-// slice of the group's (row, 4 dims) items from all the cluster's partials
-// in ascending shard (= cluster rank) order with merge_group's arithmetic
-// (max, then c_s = 2^(m_s - M) with fused multiply-adds), so the bits equal
-// the workspace merge's; a second barrier keeps every CTA's shared memory
-// alive until the last read.
-template <int D, int NT8, class E>
-__device__ __forceinline__ void cluster_merge(const SplitArgs& a) {
-  using P = ClusterPartial<D, NT8>;
-  constexpr int kQuads = D / 4;
-  __syncwarp();
-  cluster_sync_all();
-  const uint32_t S = cluster_size(), rank = cluster_rank();
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int R = a.T * a.G, total = R * kQuads;
-  const int per = (total + (int)S - 1) / (int)S;
-  const int e_end = min(total, ((int)rank + 1) * per);
-  uint8_t* base = ring_base();
-  for (int e = (int)rank * per + (int)threadIdx.x; e < e_end; e += (int)blockDim.x) {
-    const int g = e / kQuads, q = e % kQuads;
-    const float2* ml_local = reinterpret_cast<const float2*>(base + P::kMlOffset) + g;
-    const float* o_local = reinterpret_cast<const float*>(base + P::kOutOffset) + g * D + 4 * q;
-    float M = -INFINITY;
-    bool z = false;
-    for (uint32_t j = 0; j < S; ++j) {
-      const float2 v = ld_dsmem_f2(dsmem_addr(ml_local, j));
-      z |= v.y < 0.f;  // a shard saw a bad page or gave up waiting
-      M = fmaxf(M, v.x);
-    }
-    z |= M == -INFINITY;  // no shard holds a position of this row
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t j = 0; !z && j < S; ++j) {
-      const float2 v = ld_dsmem_f2(dsmem_addr(ml_local, j));
-      const float4 x = ld_dsmem_f4(dsmem_addr(o_local, j));
-      const float c = fast_exp2(v.x - M);
-      L = __fmaf_rn(c, v.y, L);
-      o.x = __fmaf_rn(c, x.x, o.x);
-      o.y = __fmaf_rn(c, x.y, o.y);
-      o.z = __fmaf_rn(c, x.z, o.z);
-      o.w = __fmaf_rn(c, x.w, o.w);
-    }
-    z |= L == 0.f;
-    const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
-    const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
-    const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
-    if (PGD_IN(row, (size_t)a.batch * a.T * a.Hq, a.err)) {
-      uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * q);
-      dst[0] = lo;
-      dst[1] = hi;
-    }
-  }
-  cluster_sync_all();
 }
 
 // The split kernel with the deep ring.  Its launch bounds name no CTA count:
-// the register allocation it gets that way (128 at D = 128 with one n8 tile,
-// 166 with two) leaves two CTAs per SM; naming one CTA per SM instead gave
-// the two-tile kernel 205 registers, one CTA per SM and a 20 % slower T = 2
-// long step.
+// the register allocation it gets that way leaves two CTAs per SM at
+// D <= 128.
 template <int D, int NT8, class E>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -678,7 +764,6 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel_cluster(const __grid_constant__ CUtensorMap tmap_k,
                              const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
   split_mma_body<D, NT8, E, false, true>(tmap_k, tmap_v, a);
-  cluster_merge<D, NT8, E>(a);
 }
 
 // The split kernel with the shallow ring: registers capped for 3 CTAs per SM.

@@ -49,6 +49,7 @@ struct SplitArgs {
   int32_t head_fastest;       // grid (Hkv, S, B) when set, else (S, Hkv, B)
   int32_t stall_tx;           // 0; a test sets extra bytes on the first stage's barrier
   int32_t batch;              // B (the checked build's bounds)
+  int32_t len_hint;           // the plan's bound on seq_lens (the speculative page-id read)
   float scale_log2;           // scale * log2(e)
 };
 
@@ -149,22 +150,27 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
 // CTA's partial is written: the last CTA of the group to finish (an atomic
 // ticket; no CTA ever waits on another) merges the group's partials into the
 // output in ascending shard order and clears the ticket for the next call.
+// The ticket is one acquire-release atomic of thread 0 after a barrier of
+// the writing threads: its release publishes the whole CTA's partial (the
+// barrier orders the other threads' writes before it), and in the last CTA
+// its acquire, passed on by the next barrier, makes every other CTA's
+// partial visible to the merge.
 template <int D, class E = __half>
 __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange& r, int b, int h,
                                               uint8_t* smem, int nthreads) {
   __shared__ int is_last_s;
-  __threadfence();  // this thread's partial writes, visible GPU-wide
-  named_barrier_sync(1, nthreads);
+  named_barrier_sync(1, nthreads);  // every thread's partial writes are issued
   int32_t* ticket = a.counters + (size_t)b * a.Hkv + h;
   if (!PGD_IN((size_t)b * a.Hkv + h, (size_t)a.batch * a.Hkv, a.err)) return;
   if (threadIdx.x == 0) {
-    const int old = atomicAdd(ticket, 1);
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket)
+                 : "memory");
     if (old < 0 || old >= r.nshards) raise_error(a.err, DECODE_ATTN_DEV_WORKSPACE);
     is_last_s = old == r.nshards - 1;
   }
   named_barrier_sync(1, nthreads);
   if (!is_last_s) return;
-  __threadfence();
   CombineArgs c{};
   c.seq_lens = a.seq_lens;
   c.ws_acc = a.ws_acc;

@@ -305,26 +305,6 @@ def test_bf16_plans(pkg):
             pkg.decode_attn_make_plan(params(pkg, **bad), 152)
 
 
-def test_persistent_plans(pkg):
-    long_p = dict(batch=4, num_q_heads=64, num_kv_heads=8, page_size=64,
-                  max_pages_per_seq=2048, num_pages=8192, max_seq_len=131072)
-    assert pkg.decode_attn_make_plan(params(pkg, **long_p), 152).persistent == 0  # auto: grid
-    plan = pkg.decode_attn_make_plan(params(pkg, **long_p, schedule=2), 152)
-    assert plan.persistent == 1 and plan.grid_x == 152 * plan.ctas_per_sm
-    assert plan.grid_y == plan.grid_z == 1 and plan.ctas_per_sm == 2
-    rows = plan.grid_x * 2 * 8  # two partial slots of G rows per CTA
-    assert plan.workspace_bytes >= 65536 + rows * (128 + 2) * 4
-    # the CUDA-core variant cannot run it
-    with pytest.raises(pkg.DecodeAttnError):
-        pkg.decode_attn_make_plan(params(pkg, **long_p, variant=1, schedule=2), 152)
-    # small work stays on the grid unless asked
-    assert pkg.decode_attn_make_plan(params(pkg), 152).persistent == 0
-    assert pkg.decode_attn_make_plan(params(pkg, schedule=2), 152).persistent == 1
-    with pytest.raises(pkg.DecodeAttnError) as e:
-        pkg.decode_attn_make_plan(params(pkg, batch=1025, schedule=2), 152)
-    assert e.value.code == -10
-
-
 @pytest.mark.parametrize("D,Hq,Hkv,stages", [(128, 32, 8, 2), (64, 32, 8, 4), (64, 64, 4, 4),
                                              (128, 64, 4, None), (256, 16, 4, None)])
 def test_shallow_ring_for_many_short_shards(pkg, D, Hq, Hkv, stages):
@@ -378,7 +358,7 @@ def test_environment_sets_the_planner_defaults():
 
 
 def test_cluster_plans(pkg):
-    """One-wave tensor-core split plans of 2..8 shards merge inside a
+    """One-wave tensor-core split plans of 2..16 shards merge inside a
     thread-block cluster when the grid fills most CTA slots or the step is
     small; the grid schedule and longer shard lists merge through the
     workspace; asking for a cluster where none applies is an error."""
@@ -391,44 +371,15 @@ def test_cluster_plans(pkg):
     plan = pkg.decode_attn_make_plan(params(pkg, **long4, schedule=1), 152)
     assert plan.cluster == 0
     plan = pkg.decode_attn_make_plan(params(pkg), 152)   # Llama shape: 16 shards
-    assert plan.max_shards > 8 and plan.cluster == 0
-    with pytest.raises(pkg.DecodeAttnError):
-        pkg.decode_attn_make_plan(params(pkg, schedule=3), 152)
-    plan = pkg.decode_attn_make_plan(params(pkg, schedule=3, force_chunk=384), 152)
+    assert plan.cluster == plan.max_shards == 16
+    with pytest.raises(pkg.DecodeAttnError):                  # 24 shards
+        pkg.decode_attn_make_plan(params(pkg, schedule=2, force_chunk=128), 152)
+    plan = pkg.decode_attn_make_plan(params(pkg, schedule=2, force_chunk=384), 152)
     assert plan.cluster == plan.max_shards == 8
+    plan = pkg.decode_attn_make_plan(params(pkg, schedule=1), 152)
+    assert plan.cluster == 0 and plan.max_shards == 16
     # a sparse grid of clusters (128 CTAs, 537 MB) keeps the workspace merge
     plan = pkg.decode_attn_make_plan(
         params(pkg, batch=2, num_q_heads=64, page_size=64, max_pages_per_seq=1024,
                num_pages=2048, max_seq_len=65536, force_chunk=8192), 152)
     assert plan.max_shards == 8 and plan.cluster == 0
-
-
-def test_all_heads_plans(pkg):
-    """The all-heads schedule, on request, on the shapes its kernel serves
-    (tensor cores, D 64/128, 8 KV heads, G <= 8, T = 1, pages of 16 or more):
-    one CTA per SM, shards of 256..1024 positions; the planner never picks it
-    by itself; asking for it where it does not apply is an error."""
-    batched = dict(batch=64, max_pages_per_seq=512, num_pages=20000, max_seq_len=8192)
-    assert pkg.decode_attn_make_plan(params(pkg, **batched), 152).all_heads == 0
-    batched["schedule"] = 4
-    plan = pkg.decode_attn_make_plan(params(pkg, **batched), 152)
-    assert plan.all_heads == 1 and plan.split == 1 and plan.grid_x == 152
-    assert plan.grid_y == plan.grid_z == 1 and plan.cluster == 0 and plan.tile_tokens == 16
-    assert plan.chunk_tokens == 512 and plan.max_shards == 16 and plan.ring_stages == 3
-    tickets = max(64 * 1024, ((64 * 8 + 64) * 4 + 255) // 256 * 256)
-    assert plan.workspace_bytes == tickets + 64 * 32 * 16 * 8 + 64 * 32 * 16 * 128 * 4
-    plan = pkg.decode_attn_make_plan(params(pkg, **batched, head_dim=64), 152)
-    assert plan.all_heads == 1 and plan.ring_stages == 6
-    many = dict(batch=1000, max_pages_per_seq=32, num_pages=40000, max_seq_len=512, schedule=4)
-    plan = pkg.decode_attn_make_plan(params(pkg, **many), 152)
-    assert plan.all_heads == 1 and plan.chunk_tokens == 256 and plan.max_shards == 2
-    assert pkg.decode_attn_make_plan(params(pkg), 152).all_heads == 0            # Llama shape
-    for kw in (dict(head_dim=256), dict(num_q_heads=16, num_kv_heads=4), dict(num_queries=2),
-               dict(num_q_heads=128), dict(page_size=8, max_pages_per_seq=1024),
-               dict(force_chunk=2048), dict(variant=1)):
-        with pytest.raises(pkg.DecodeAttnError):
-            pkg.decode_attn_make_plan(params(pkg, **{**batched, **kw}), 152)
-    plan = pkg.decode_attn_make_plan(params(pkg, schedule=4), 152)   # forced on a small step
-    assert plan.all_heads == 1 and plan.max_shards == math.ceil(3060 / plan.chunk_tokens)
-    plan = pkg.decode_attn_make_plan(params(pkg, **batched, force_chunk=300), 152)
-    assert plan.chunk_tokens == 320 and plan.max_shards == math.ceil(8192 / 320)

@@ -33,7 +33,7 @@ from paged_gqa_decode_06_gb300 import workloads
 
 DEV = "cuda:0"
 BARS = {torch.float16: (5e-4, 2e-3, 1e-3), torch.bfloat16: (3e-3, 1e-2, 6e-3)}
-GRID, CLUSTER = 1, 3
+GRID, CLUSTER = 1, 2
 
 # path -> (shape, lengths, call keywords)
 PATHS = {
@@ -73,7 +73,7 @@ def check_plan(pkg, path, params):
     if path == "single":
         assert plan.split == 0
     elif path == "grid":
-        assert plan.split == 1 and plan.cluster == 0 and plan.persistent == 0
+        assert plan.split == 1 and plan.cluster == 0
     elif path == "cluster":
         assert plan.split == 1 and plan.cluster >= 2
     else:  # the shallow ring: 2 stages of 64 tokens at D = 128, several waves

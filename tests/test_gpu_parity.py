@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 REL_L2, MAX_ABS, ROW_REL = 5e-4, 2e-3, 1e-3
 SIMT, MMA = 1, 2
+GRID = 1  # the grid schedule: every split plan merges through the workspace
 VARIANTS = pytest.mark.parametrize("variant", [SIMT, MMA], ids=["simt", "mma"])
 
 
@@ -415,22 +416,27 @@ def test_more_shards_than_one_staged_block(pkg, variant):
 
 def test_dirty_workspace_is_detected_and_clearable(pkg):
     """Shard tickets that are not zero on entry raise DEV_WORKSPACE (the
-    group's rows may then be stale); decode_attn_workspace_clear fixes it."""
+    group's rows may then be stale); decode_attn_workspace_clear fixes it.
+    The grid schedule is the one that merges through tickets (cluster plans
+    merge inside their clusters).  Detection is best-effort: the last arrival
+    resets a ticket, so later arrivals may land in range again."""
     w = workloads.make("llama", device=DEV)
-    ref, _ = run(pkg, w)
-    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len())
+    ref, _ = run(pkg, w, schedule=GRID)
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len(),
+                             schedule=GRID)
     ws = torch.full((pkg.decode_attn_workspace_size(params, 0),), 0x7F, dtype=torch.uint8,
                     device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
-                    max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err)
+                    max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err, schedule=GRID)
     torch.cuda.synchronize()
     assert int(err.item()) & pkg.DEV_WORKSPACE
     pkg.decode_attn_workspace_clear(params, ws)
     err.zero_()
     for _ in range(2):  # a completed call leaves the tickets clear
         out = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
-                              max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err)
+                              max_seq_len=w.max_seq_len(), workspace=ws, err_flag=err,
+                              schedule=GRID)
         torch.cuda.synchronize()
         assert int(err.item()) == 0 and torch.equal(out, ref)
 

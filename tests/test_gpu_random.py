@@ -2,7 +2,7 @@
 sizes, query positions, page sizes, batch and length mixes (zeros included),
 windows, element formats, variants and schedules drawn together, so the
 planner's choices (single pass, split, one wave or several, deep or shallow
-ring, persistent) meet the kernels in combinations the fixed cases do not."""
+ring, workspace or cluster merge) meet the kernels in combinations the fixed cases do not."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +43,7 @@ def draw(seed):
     window = int(rng.integers(1, lmax + 1)) if rng.random() < 0.3 else 0
     dtype = torch.bfloat16 if rng.random() < 0.3 else torch.float16
     variant = 1 if (T == 1 and G <= 8 and dtype == torch.float16 and rng.random() < 0.2) else 2
-    schedule = 2 if (variant == 2 and rng.random() < 0.15) else 0
+    schedule = 1 if (variant == 2 and rng.random() < 0.15) else 0  # the workspace merge
     split_min = int(rng.choice([0, 0, 0, 1, 100000]))
     force_chunk = int(rng.choice([0, 0, 0, 0, 64, 192, 1024]))
     return dict(D=D, Hkv=Hkv, G=G, T=T, PS=PS, B=B, lens=lens.tolist(), window=window,
