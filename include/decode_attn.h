@@ -132,6 +132,10 @@ typedef struct decode_attn_plan {
   int32_t cluster;           /* CTAs per thread-block cluster (the shards of one
                                 (KV head, sequence), merged through distributed shared
                                 memory; 2..16), or 0 (merged through the workspace) */
+  int32_t balanced;          /* 1: each sequence's attended range is cut into max_shards
+                                near-equal shards of whole 64-position tiles (chunk_tokens
+                                is then an upper bound); 0: shards of chunk_tokens
+                                positions (one-wave split plans take 1) */
   size_t workspace_bytes;    /* tickets max(64 KiB, (B*Hkv+64)*4) + partials B*Hq*S_max*(D+2)*4,
                                 each part rounded up to 256 B; 0 for a single-pass plan */
 } decode_attn_plan;

@@ -61,7 +61,7 @@ class DecodeAttnPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "split", "variant", "group_pad", "tile_tokens", "chunk_tokens", "max_shards",
         "grid_x", "grid_y", "grid_z", "ctas_per_sm", "head_fastest", "ring_stages",
-        "cluster")] + [
+        "cluster", "balanced")] + [
         ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):

@@ -280,6 +280,11 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   const int64_t slots_all = (int64_t)num_sms * cps;
   const bool head_fastest = ctas > slots_all;
   plan->head_fastest = head_fastest ? 1 : 0;
+  // one-wave split plans cut each sequence into max_shards near-equal
+  // shards: all CTAs run at once, so the step lasts as long as the longest
+  // shard (a 4096-position window on 64-aligned lengths: 8 x 512 positions
+  // instead of 7 x 576 + 64); a forced chunk is taken as given
+  plan->balanced = (plan->split && !head_fastest && force_chunk <= 0) ? 1 : 0;
   plan->grid_x = head_fastest ? p->num_kv_heads : (int32_t)max_shards;
   plan->grid_y = head_fastest ? (int32_t)max_shards : p->num_kv_heads;
   plan->grid_z = p->batch;
@@ -454,6 +459,7 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
   a.window = p->window > 0 ? p->window : 0;
   a.chunk = plan.chunk_tokens;
   a.max_shards = plan.max_shards;
+  a.balanced = plan.balanced;
   a.split = plan.split;
   a.T = num_queries(p);
   a.head_fastest = plan.head_fastest;
@@ -508,6 +514,7 @@ int run_combine(const decode_attn_params* p, const decode_attn_plan& plan,
   a.window = p->window > 0 ? p->window : 0;
   a.chunk = plan.chunk_tokens;
   a.max_shards = plan.max_shards;
+  a.balanced = plan.balanced;
   switch (p->head_dim) {
     case 64: return cuda_status(launch_combine_d64(a, p->dtype, stream));
     case 128: return cuda_status(launch_combine_d128(a, p->dtype, stream));

@@ -25,7 +25,7 @@ struct CombineArgs {
   const float2* ws_ml;   // [B*T*Hq*S_max]
   void* out;             // [B][T][Hq][D] 16-bit elements
   int32_t* err;          // nullable; the checked build's bounds errors
-  int32_t B, Hq, G, T, capacity, window, chunk, max_shards;
+  int32_t B, Hq, G, T, capacity, window, chunk, max_shards, balanced;
 };
 
 // Bounds of the partial slots (the checked build).
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
   const int h = blockIdx.x, b = blockIdx.y;
   grid_dependency_wait();  // the lengths and partials may come from the kernel before
   const SeqRange r =
-      seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T);
+      seq_range(a.seq_lens[b], a.window, a.capacity, a.chunk, a.max_shards, a.T, a.balanced);
   merge_group<D, E>(a, b, h, r.nshards, r.status != 0, threadIdx.x, blockDim.x, merge_smem,
                     kShardBlock, [] { __syncthreads(); },
                     GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});

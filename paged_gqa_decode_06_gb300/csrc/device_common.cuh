@@ -50,6 +50,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// A 32-bit global load the compiler keeps in program order with the other
+// asm loads (so two independent loads go out back to back).
+__device__ __forceinline__ int32_t ld_global_s32(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -123,15 +131,21 @@ struct SeqRange {
   int32_t start;    // first attended position
   int32_t end;      // one past the last attended position (= seq_len)
   int32_t base;     // start rounded down to a multiple of kTile
+  int32_t chunk;    // positions per shard (a multiple of kTile)
   int32_t nshards;  // shards holding attended positions (0 for an empty range)
   int32_t status;   // 0 or DECODE_ATTN_DEV_* bits
 };
 
 // With T query positions per sequence (the last T positions), the range is
 // the union of the queries' ranges: the first query's window start to L.
+// balanced: the range is cut into max_shards near-equal shards (the planned
+// chunk is then an upper bound), so that no shard of a sequence is much
+// shorter than the others; otherwise every shard but the last has `chunk`
+// positions.
 __device__ __forceinline__ SeqRange seq_range(int32_t L, int32_t window, int32_t capacity,
-                                              int32_t chunk, int32_t max_shards, int32_t T = 1) {
-  SeqRange r{0, 0, 0, 0, 0};
+                                              int32_t chunk, int32_t max_shards, int32_t T = 1,
+                                              int32_t balanced = 0) {
+  SeqRange r{0, 0, 0, chunk, 0, 0};
   if (L < 0 || L > capacity) {
     r.status = DECODE_ATTN_DEV_BAD_LEN;
     return r;
@@ -140,7 +154,11 @@ __device__ __forceinline__ SeqRange seq_range(int32_t L, int32_t window, int32_t
   const int32_t first_end = L - T + 1;  // one past the first query's position
   r.start = (window > 0 && first_end > window) ? first_end - window : 0;
   r.base = r.start & ~(kTile - 1);
-  r.nshards = (L > r.start) ? (L - r.base + chunk - 1) / chunk : 0;
+  if (balanced && L > r.base && max_shards > 0) {
+    const int32_t even = (L - r.base + max_shards - 1) / max_shards;
+    r.chunk = min(chunk, max(kTile, (even + kTile - 1) & ~(kTile - 1)));
+  }
+  r.nshards = (L > r.start) ? (L - r.base + r.chunk - 1) / r.chunk : 0;
   if (r.nshards > max_shards) {
     r.status = DECODE_ATTN_DEV_OVER_HINT;
     r.nshards = 0;

@@ -243,8 +243,11 @@ __device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
   asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
                : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -311,8 +314,13 @@ __device__ __forceinline__ void cluster_finish(const SplitArgs& a, const Cluster
                                                int h, uint32_t recv_bar, uint8_t* recv,
                                                int nthreads) {
   named_barrier_sync(1, nthreads);  // every consumer's stores are issued
-  if (threadIdx.x == 0)
-    for (int o = 0; o < x.S; ++o) mbar_arrive_remote_release(dsmem_addr(recv_bar, (uint32_t)o));
+  // thread o announces this CTA's partial to owner o: a cluster-scope release
+  // fence (it orders the stores the barrier above ordered before it) and a
+  // relaxed arrival on the owner's receive barrier
+  if ((int)threadIdx.x < x.S) {
+    fence_acq_rel_cluster();
+    mbar_arrive_remote_relaxed(dsmem_addr(recv_bar, threadIdx.x));
+  }
   // this CTA's slice: wait for the S partials, merge in shard order
   __shared__ int recv_ok_s;
   if (threadIdx.x == 0) {
@@ -428,16 +436,19 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   int spec_lo = -1, spec_phys = -1;
   if (warp == kWarps) {
     const SeqRange g =
-        seq_range(a.len_hint, a.window, capacity, a.chunk, a.max_shards, a.T);
+        seq_range(a.len_hint, a.window, capacity, a.chunk, a.max_shards, a.T, a.balanced);
     if (g.status == 0 && s < g.nshards) {
-      spec_lo = g.base + s * a.chunk;
+      spec_lo = g.base + s * g.chunk;
       const int ptok = spec_lo + lane * box_t;
       const size_t pi = (size_t)b * a.max_pages + (ptok >> a.page_shift);
       if (ptok < capacity && PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err))
-        spec_phys = a.page_table[pi];
+        spec_phys = ld_global_s32(a.page_table + pi);
     }
   }
-  const SeqRange r = seq_range(a.seq_lens[b], a.window, capacity, a.chunk, a.max_shards, a.T);
+  // (ld_global_s32 keeps the two loads in this order, both in flight at once)
+  const SeqRange r =
+      seq_range(ld_global_s32(a.seq_lens + b), a.window, capacity, a.chunk, a.max_shards, a.T,
+                a.balanced);
   const int R = a.T * a.G;  // query rows of the group: r = t * G + g
   const int gid = lane >> 2, tig = lane & 3;
 
@@ -462,9 +473,9 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     return;
   }
 
-  const int shard_lo = r.base + s * a.chunk;
+  const int shard_lo = r.base + s * r.chunk;
   const int lo = max(r.start, shard_lo);
-  const int hi = min(r.end, shard_lo + a.chunk);
+  const int hi = min(r.end, shard_lo + r.chunk);
   const int n_tiles = (hi - shard_lo + kTile - 1) / kTile;
   const int pieces_per_tile = kTile / box_t;
   const int n_pieces = n_tiles * pieces_per_tile;
@@ -503,7 +514,6 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
         tma_load_4d_hint(dst + dc * (kTile * 128), map, 0, coord, h, dc, fb, policy);
     }
   };
-  bool bad = false;
   if (warp == kWarps) {
     // physical coordinates of every box of the shard
     int any_bad = 0;
@@ -528,17 +538,43 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
       }
       coord_s[i] = coord;
     }
-    bad = __any_sync(0xffffffffu, any_bad) != 0;
-    if (lane == 0 && bad) {
-      bad_s = 1;
-      raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
-    }
-    if (!bad) {
-      if (a.k_new != nullptr && r.end - a.T < shard_lo + a.chunk && r.end > shard_lo)
+    const bool bad = __any_sync(0xffffffffu, any_bad) != 0;
+    if (bad) {
+      // no copy is issued; the consumers' first wait completes on a plain
+      // arrival and they find the flag
+      if (lane == 0) {
+        bad_s = 1;
+        raise_error(a.err, DECODE_ATTN_DEV_BAD_PAGE);
+        mbar_arrive(smem_u32(&full_bar[0]));
+      }
+    } else {
+      if (a.k_new != nullptr && r.end - a.T < shard_lo + r.chunk && r.end > shard_lo)
         append_new_rows<D>(a, r, b, h, shard_lo, lane);
       const uint64_t policy = l2_evict_first_policy();
-      for (int i = 0; i < min(n_tiles, C::kStages); ++i) issue_stage(i, policy);
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        if (i >= C::kStages) {
+          const int st = i % C::kStages;
+          int go = 1;
+          if (lane == 0) {
+            if (!mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) & 1) ^ 1)) {
+              abort_s = 1;
+              raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
+              go = 0;
+            }
+            if (abort_s) go = 0;
+          }
+          if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        }
+        issue_stage(i, policy);
+        issued = i + 1;
+      }
+      // drain this CTA's copies in flight before the warp exits
+      if (lane == 0)
+        for (int i = max(0, issued - C::kStages); i < issued; ++i)
+          mbar_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
     }
+    return;
   }
 
   // ------------------------------------------------ consumers' set-up
@@ -585,46 +621,16 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
   }
-  __syncthreads();  // the page ids and the bad-page flag are in shared memory
-  bad = bad_s != 0;
-
-  if (warp == kWarps) {
-    if (!bad) {
-      const uint64_t policy = l2_evict_first_policy();
-      int issued = min(n_tiles, C::kStages);
-      for (int i = C::kStages; i < n_tiles; ++i) {
-        const int st = i % C::kStages;
-        int go = 1;
-        if (lane == 0) {
-          if (!mbar_wait(smem_u32(&empty_bar[st]), ((i / C::kStages) & 1) ^ 1)) {
-            abort_s = 1;
-            raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
-            go = 0;
-          }
-          if (abort_s) go = 0;
-        }
-        if (!__shfl_sync(0xffffffffu, go, 0)) break;
-        issue_stage(i, policy);
-        issued = i + 1;
-      }
-      // drain this CTA's copies in flight before the warp exits
-      if (lane == 0)
-        for (int i = max(0, issued - C::kStages); i < issued; ++i)
-          mbar_wait(smem_u32(&full_bar[i % C::kStages]), (i / C::kStages) & 1);
-    }
-    return;
-  }
-
   // ------------------------------------------------------------ consumers
   const int piece_shift = __ffs(box_t) - 1;  // a stage is pieces of box_t rows
-  for (int i = 0; i < n_tiles && !bad; ++i) {
+  for (int i = 0; i < n_tiles; ++i) {
     const int st = i % C::kStages;
     if (!mbar_wait(smem_u32(&full_bar[st]), (i / C::kStages) & 1)) {
       abort_s = 1;
       raise_error(a.err, DECODE_ATTN_DEV_TIMEOUT);
       break;
     }
-    if (abort_s) break;
+    if (bad_s || abort_s) break;
     const int tok0 = shard_lo + i * kTile + 16 * warp;  // this warp's 16 positions
     if (tok0 + 16 > lo && tok0 < hi)
       mma_block<D, NT8, E>(ring + st * C::kStageBytes, warp, lane, tok0, lo, hi, col_lo, col_hi,
@@ -688,7 +694,7 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
     row_s[g] = make_float2(M, L);
   }
   named_barrier_sync(1, kWarps * 32);
-  const bool dead = bad || abort_s != 0;
+  const bool dead = bad_s != 0 || abort_s != 0;
   uint8_t* recv = ring + C::kRingBytes;  // a cluster plan's receive buffer
   ClusterXchg x;
   if constexpr (CL) {

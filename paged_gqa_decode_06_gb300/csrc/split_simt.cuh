@@ -45,6 +45,7 @@ struct SplitArgs {
   int32_t Hq, Hkv, G;
   int32_t max_pages, num_pages, page_size, page_shift, box_tokens;
   int32_t window, chunk, max_shards, split;
+  int32_t balanced;           // shards of each sequence of near-equal length (seq_range)
   int32_t T;                  // query positions per sequence (1 for the CUDA-core variant)
   int32_t head_fastest;       // grid (Hkv, S, B) when set, else (S, Hkv, B)
   int32_t stall_tx;           // 0; a test sets extra bytes on the first stage's barrier
@@ -123,7 +124,7 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
                                                 int h, int shard_lo, int lane) {
   for (int i = 0; i < a.T; ++i) {
     const int pos = r.end - a.T + i;  // position of the i-th new token
-    if (pos < shard_lo || pos >= shard_lo + a.chunk || pos < 0) continue;
+    if (pos < shard_lo || pos >= shard_lo + r.chunk || pos < 0) continue;
     const size_t pi = (size_t)b * a.max_pages + (pos >> a.page_shift);
     if (!PGD_IN(pi, (size_t)a.batch * a.max_pages, a.err)) continue;
     const int phys = a.page_table[pi];
@@ -184,6 +185,7 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   c.capacity = a.max_pages * a.page_size;
   c.window = a.window;
   c.chunk = a.chunk;
+  c.balanced = a.balanced;
   c.max_shards = a.max_shards;
   merge_group<D, E>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem, kShardBlock,
                     [nthreads] { named_barrier_sync(1, nthreads); },
@@ -227,7 +229,7 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqRange r = seq_range(a.seq_lens[b], a.window, a.max_pages * a.page_size, a.chunk,
-                               a.max_shards, a.T);
+                               a.max_shards, a.T, a.balanced);
   if (r.status != 0 || s >= r.nshards) {
     // nothing to stream: report a bad length once; shard 0 owns the group's
     // output rows (zero for an empty or invalid range)
@@ -238,9 +240,9 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
     return;
   }
 
-  const int shard_lo = r.base + s * a.chunk;  // tile-aligned absolute position
+  const int shard_lo = r.base + s * r.chunk;  // tile-aligned absolute position
   const int lo = max(r.start, shard_lo);
-  const int hi = min(r.end, shard_lo + a.chunk);
+  const int hi = min(r.end, shard_lo + r.chunk);
   const int n_tiles = (hi - shard_lo + kTile - 1) / kTile;
   const int box_t = a.box_tokens;
   const int pieces_per_tile = kTile / box_t;
@@ -284,8 +286,8 @@ __global__ void __launch_bounds__(SimtCfg<D>::kThreads)
 
   if (warp == kWarps) {
     if (a.k_new != nullptr && !bad) {
-      const int shard_lo_w = r.base + s * a.chunk;
-      if (r.end - a.T < shard_lo_w + a.chunk && r.end > shard_lo_w)
+      const int shard_lo_w = r.base + s * r.chunk;
+      if (r.end - a.T < shard_lo_w + r.chunk && r.end > shard_lo_w)
         append_new_rows<D>(a, r, b, h, shard_lo_w, lane);
     }
     if (lane == 0 && !bad) {
