@@ -41,6 +41,7 @@ WORKLOAD_DESC = {
     "long": "B=4, seq 131072 each, Hq=64, Hkv=8, D=128, page 64, full context",
     "long_b1": "B=1, seq 131072, Hq=64, Hkv=8, D=128, page 64, full context",
     "long_w4096": "B=4, seq 131072 each, Hq=64, Hkv=8, D=128, page 64, window 4096",
+    "long_d256": "B=1, seq 131072, Hq=16, Hkv=4, D=256, page 64, full context",
     "batched": "B=64, Hq=32, Hkv=8, D=128, seq_lens U[1,8192], page 16",
     "llama": "B=1, Hq=32, Hkv=8, D=128, context 3060, page 16 (Llama-3.1-8B shape)",
     "sweep_d64": "B=1, Hq=32, Hkv=8, D=64, context 3060, page 16",
@@ -458,8 +459,11 @@ def gpu_arm(args):
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     resident = (w.k_pages.numel() + w.v_pages.numel()) * 2
     flush, l2_desc = l2_policy(kv_bytes, l2)
-    flush_buf = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
-    flush_read = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev)
+    # the flush buffers: for this workload when it fits in twice the L2, and
+    # for the per_config block's small workloads
+    need_flush = flush or args.config_steps > 0
+    flush_buf = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev) if need_flush else None
+    flush_read = torch.ones(4 * l2 // 4, dtype=torch.float32, device=dev) if need_flush else None
 
     def flush_l2():
         # write 4x L2 (evicts the step's data), then read another 4x L2 so the

@@ -26,7 +26,17 @@ constexpr int kMaxCluster = 16;  // largest thread-block cluster (above 8: non-p
 // two and four sequences of 16 Ki..128 Ki tokens, the Llama-3.1-8B shape, the
 // windowed long case):
 constexpr double kStreamBytesPerS = 7.0e12;  // sustained K/V read rate of the split kernel
-constexpr double kRoundTripS = 2.0e-6;       // loaded latency: a CTA moves its ring once per trip
+constexpr double kRoundTripS = 3.0e-6;       // loaded latency: a CTA moves its ring once per trip
+// One-wave grids are kept to about this share of the CTA slots: with every
+// slot filled, each SM runs two CTAs and the shared SMs' CTAs finish last
+// (GB300: one 131072-token sequence 89.1 us at 256 CTAs against 94.3 us at
+// 304; two of 65536 87.5 against 90.0; the long case 302.7 at 256).
+constexpr double kOneWaveFill = 0.85;
+// Clusters above the portable 8 CTAs only for grids this small: larger grids
+// of 9..16-CTA clusters cannot be packed onto the GPCs (two 65536-token
+// sequences in 16-CTA clusters: 133 us against 87.5 us merging through the
+// workspace; the head_dim-256 sweep shape, 64 CTAs: 16.3 against 18.3 us).
+constexpr int64_t kLargeClusterMaxCtas = 64;
 constexpr double kMergeStepS = 1.2e-6;       // the last CTA's merge: one L2 round trip per 8 shards
 
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -145,8 +155,9 @@ int64_t one_wave_shards(int64_t units, int64_t slots, int64_t span, int head_dim
   const double bytes = (double)units * (double)span * 4.0 * head_dim;
   // above the split threshold the step is split: at least two shards
   const int64_t s_lo = std::max<int64_t>(2, ceil_div(span, max_chunk));
-  const int64_t s_hi =
-      std::max<int64_t>(s_lo, std::min<int64_t>(slots / units, ceil_div(span, kMinChunk)));
+  const int64_t fill = std::max<int64_t>(1, (int64_t)(kOneWaveFill * (double)slots) / units);
+  const int64_t s_hi = std::max<int64_t>(
+      s_lo, std::min<int64_t>(std::min<int64_t>(slots / units, fill), ceil_div(span, kMinChunk)));
   int64_t best = s_lo;
   double best_t = 1e300;
   for (int64_t S = s_lo; S <= s_hi; ++S) {
@@ -297,7 +308,9 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
   // packed onto neighbouring SMs of one GPC, so a sparse grid of clusters
   // leaves SMs idle.
   const bool cluster_ok = variant == DECODE_ATTN_VARIANT_MMA && plan->split && !head_fastest &&
-                          !shallow && max_shards >= 2 && max_shards <= kMaxCluster;
+                          !shallow && max_shards >= 2 &&
+                          (max_shards <= 8 || (max_shards <= kMaxCluster &&
+                                               ctas <= kLargeClusterMaxCtas));
   const int64_t step_bytes =
       (int64_t)p->batch * p->num_kv_heads * span * 4 * p->head_dim;
   if (p->schedule == DECODE_ATTN_SCHEDULE_CLUSTER) {

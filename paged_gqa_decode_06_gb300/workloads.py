@@ -149,6 +149,10 @@ CONFIGS = {
                     seq_lens=[131072], seed=4),
     "long_w4096": dict(batch=4, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
                        seq_lens=[131072] * 4, seed=4, window=4096),
+    # the head_dim-256 sweep shape (16/4 heads) at one 131072-token sequence:
+    # 512 MiB of K+V, above L2, for DRAM-level profiles at D = 256
+    "long_d256": dict(batch=1, num_q_heads=16, num_kv_heads=4, head_dim=256, page_size=64,
+                      seq_lens=[131072], seed=8),
 }
 
 # shapes of the short-context sweep (contexts 1..512, threshold at 256)

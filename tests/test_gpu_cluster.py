@@ -49,11 +49,12 @@ def check(out, ref, dtype):
 
 @pytest.mark.parametrize("D,Hq,Hkv,PS,lens,window,T,dtype,chunk", [
     (128, 32, 8, 16, [3060], 0, 1, torch.float16, 384),            # Llama shape, 8 shards
-    (64, 32, 8, 16, [3060], 0, 1, torch.float16, 0),               # planner's 8 shards
+    (64, 32, 8, 16, [3060], 0, 1, torch.float16, 384),             # D = 64, 8 shards
     (256, 16, 4, 16, [3060], 0, 1, torch.bfloat16, 512),           # D = 256
     (128, 64, 8, 64, [9000, 300, 0, 4097], 0, 1, torch.float16, 0),  # short ones: empty shards
     (128, 64, 8, 64, [9000, 2000, 5], 700, 1, torch.float16, 0),   # window
-    (128, 16, 4, 32, [2500, 777, 1], 0, 2, torch.float16, 0),      # T = 2, 8 query rows
+    (128, 16, 4, 32, [2500, 777, 1], 0, 2, torch.float16, 320),    # T = 2, 8 query rows
+    (256, 16, 4, 16, [3060], 0, 1, torch.float16, 0),              # planner: 16 shards, 64 CTAs
     (128, 16, 2, 16, [4000, 300], 0, 2, torch.bfloat16, 512),      # T = 2, G = 8: 16 rows
     (64, 8, 8, 16, [1000, 1000], 0, 1, torch.float16, 128),        # G = 1, 8 shards
 ])
@@ -75,7 +76,7 @@ def test_cluster_parity_and_bits(pkg, D, Hq, Hkv, PS, lens, window, T, dtype, ch
                              chunk, CLUSTER)
     plan = pkg.decode_attn_make_plan(params,
                                      torch.cuda.get_device_properties(DEV).multi_processor_count)
-    assert plan.cluster == plan.max_shards and 2 <= plan.cluster <= 8, plan.as_dict()
+    assert plan.cluster == plan.max_shards and 2 <= plan.cluster <= 16, plan.as_dict()
     out_c, err_c = run(pkg, qd, wd, Ld, window, max_len, CLUSTER, force_chunk=chunk)
     out_g, err_g = run(pkg, qd, wd, Ld, window, max_len, GRID, force_chunk=chunk)
     assert err_c == 0 and err_g == 0
@@ -87,8 +88,9 @@ def test_cluster_parity_and_bits(pkg, D, Hq, Hkv, PS, lens, window, T, dtype, ch
 
 def test_cluster_split_then_combine_equals(pkg):
     """decode_attn_combine re-merges the partials a cluster launch also left
-    in the workspace: the same bits as the cluster merge."""
-    w = workloads.make("sweep_d64", device=DEV)
+    in the workspace: the same bits as the cluster merge (the head_dim-256
+    sweep shape: 16 shards in clusters of 16)."""
+    w = workloads.make("sweep_d256", device=DEV)
     params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, w.max_seq_len(), 0, 0,
                              0, CLUSTER)
     out, ws = pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,

@@ -101,7 +101,7 @@ def run_all(pkg, q, w, lens, window, T, kw):
     (128, 32, 8, 16, [3000, 40, 0, 700], 1, 0, torch.float16, 0, AUTO, V_AUTO),
     (128, 32, 8, 16, [3000, 40, 0, 700], 1, 0, torch.float16, 256, GRID, V_AUTO),
     (128, 32, 8, 16, [1500, 40, 0, 700], 1, 0, torch.float16, 512, CLUSTER, V_AUTO),
-    (128, 32, 8, 16, [3000, 700], 1, 0, torch.float16, 192, CLUSTER, V_AUTO),  # 16 CTAs
+    (128, 16, 4, 16, [3000], 1, 0, torch.float16, 192, CLUSTER, V_AUTO),  # 16-CTA clusters
     (128, 32, 8, 16, [3000, 40, 0, 700], 1, 0, torch.float16, 0, AUTO, V_SIMT),
     (128, 32, 8, 16, [200, 17, 0, 256], 1, 0, torch.float16, 0, AUTO, V_AUTO),   # single pass
     (64, 16, 4, 16, [5000, 100, 1, 333], 1, 0, torch.float16, 512, GRID, V_AUTO),
@@ -112,7 +112,7 @@ def run_all(pkg, q, w, lens, window, T, kw):
     (128, 32, 8, 16, [3000, 40, 0, 1707], 1, 700, torch.float16, 0, AUTO, V_AUTO),  # window
     (128, 32, 8, 16, [3000, 40, 0, 1707], 1, 700, torch.float16, 0, AUTO, V_SIMT),
     (128, 16, 4, 32, [2600, 90, 3, 1001], 2, 500, torch.float16, 0, GRID, V_AUTO),
-    (64, 32, 8, 32, [3000, 700], 1, 0, torch.bfloat16, 256, CLUSTER, V_AUTO),  # 12 CTAs
+    (64, 16, 4, 32, [3000], 1, 0, torch.bfloat16, 256, CLUSTER, V_AUTO),  # 12-CTA clusters
     (128, 32, 8, 16, [3000, 40, 0, 1707], 1, 700, torch.float16, 0, CLUSTER, V_AUTO),
 ])
 def test_unattended_positions_leave_no_trace(pkg, D, Hq, Hkv, PS, lens, T, window, dtype, chunk,
