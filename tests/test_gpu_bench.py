@@ -36,7 +36,7 @@ def test_bench_line_and_dump_match_the_oracle(gpu, tmp_path, name):
     path = str(tmp_path / f"{name}.npz")
     cpu = ["--cpu-budget", "1"] if name == "tiny" else ["--no-cpu-baseline"]
     (line,) = run_bench("--workload", name, "--steps", "5", "--warmup", "3", "--e2e-steps", "0",
-                        *cpu, "--dump", path)
+                        "--config-steps", "0", *cpu, "--dump", path)
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -74,3 +74,23 @@ def test_context_sweep_runs(gpu):
         if p["mode"] == "threshold 256" and p["context"] > 1:
             assert p["split"] == (1 if p["context"] > 256 else 0), p
     assert "summary_mean_us" in lines[-1]
+
+
+def test_per_config_block_and_reference_config(gpu):
+    """The default line carries every other benchmark configuration, timed the
+    same way, and the reference arm names the same configuration dict."""
+    (line,) = run_bench("--workload", "tiny", "--steps", "5", "--warmup", "3", "--e2e-steps",
+                        "0", "--no-cpu-baseline", "--config-steps", "10")
+    pc = line["per_config"]
+    assert set(pc) == {"llama", "sweep_d64", "sweep_d128", "sweep_d256", "batched", "long_w4096"}
+    peak = line["roofline"]["peak"]
+    for name, e in pc.items():
+        assert e["us_per_step"] > 0 and e["steps"] == 10, name
+        assert abs(e["frac"] - e["kv_tbs"] * 1e3 / peak) < 1e-9, name
+        assert e["kv_tbs"] * 1e12 * e["us_per_step"] * 1e-6 == pytest.approx(e["kv_bytes_per_step"],
+                                                                           rel=1e-9)
+        assert e["kernel"].startswith("split_mma_kernel"), name
+        assert 0 < e["us_percentiles"]["p10"] <= e["us_percentiles"]["p90"]
+    (ref,) = run_bench("--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup",
+                       "0")
+    assert ref["impl"] == "reference" and ref["config"] == line["config"]
