@@ -64,7 +64,8 @@ extern "C" {
 #define DECODE_ATTN_DEV_BAD_LEN 1       /* seq_len < 0 or > max_pages_per_seq * page_size */
 #define DECODE_ATTN_DEV_BAD_PAGE 2      /* page id outside [0, num_pages) in an attended range */
 #define DECODE_ATTN_DEV_OVER_HINT 4     /* seq_len beyond the max_seq_len the grid was planned for */
-#define DECODE_ATTN_DEV_TIMEOUT 8       /* a pipeline wait gave up (about 2 s); row zeroed */
+#define DECODE_ATTN_DEV_TIMEOUT 8       /* a bounded wait gave up (a pipeline wait after about
+                                           2 s, a cluster exchange after about 4 s); row zeroed */
 #define DECODE_ATTN_DEV_CHECK 32        /* checked build only (libpaged_gqa_decode_checked.so):
                                            an index fell outside its buffer; that access was
                                            skipped (or pointed at the zero-fill coordinate) */

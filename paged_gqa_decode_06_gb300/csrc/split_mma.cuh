@@ -12,8 +12,7 @@
 // Each of the four consumer warps takes 16 positions of every 64-position
 // stage; a shard's partial (running max, sum, fp32 accumulator; apache/tvm
 // pull request 20426, sharded-nest commit) is the warps' states folded in
-// fixed order.
-// The score fragment is transposed into the P^T operand with movmatrix; P is
+// fixed order.  The score fragment is transposed into the P^T operand with movmatrix; P is
 // split into a 16-bit head and a 16-bit remainder (two mma per tile), so the
 // weights keep about 22 (fp16) / 16 (bf16) bits.
 //
@@ -33,7 +32,7 @@ namespace pgd {
 // round trips overlap.
 template <int D, bool kShallow = false>
 struct MmaCfg {
-  static constexpr int kWarps = 4;  // consumer warps, D / 4 output dims apiece
+  static constexpr int kWarps = 4;  // consumer warps, 16 positions of each stage apiece
   static constexpr int kThreads = (kWarps + 1) * 32;
   static constexpr int kStages = (D == 64) ? (kShallow ? 4 : 6) : (kShallow ? 2 : 3);
   static constexpr int kTileBytes = kTile * D * 2;
@@ -167,7 +166,7 @@ __device__ __forceinline__ void mma_block(uint8_t* kt, int warp, int lane, int t
       l_part[j][e] = l_part[j][e] * alpha[j][e] + p[e] + p[e + 2];
       m_run[j][e] = m_new;
     }
-    // P^T operand: fp16 head and fp16 remainder, transposed by movmatrix
+    // P^T operand: 16-bit head and 16-bit remainder, transposed by movmatrix
     const uint32_t h0 = ElemOps<E>::pack2(p[0], p[1]);
     const uint32_t h1 = ElemOps<E>::pack2(p[2], p[3]);
     const float2 f0 = ElemOps<E>::unpack2(h0);
@@ -261,12 +260,17 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
-// Bounded like mbar_wait (about two seconds), with cluster-scope acquire.
+// Bounded like mbar_wait, with cluster-scope acquire, but after about four
+// seconds: twice the pipeline's bound.  A partner CTA reaches the exchange at
+// most one pipeline give-up (about two seconds) after its own start, so a CTA
+// that arrives first (one with an empty shard does at once) still waits for
+// it, and no CTA exits while a partner may still store into its receive
+// buffer.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait_cluster(bar, parity)) {
-    if (global_timer_ns() - t0 > 2000000000ull) return false;
+    if (global_timer_ns() - t0 > 4000000000ull) return false;
   }
   return true;
 }
@@ -483,8 +487,8 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   // Producer: the boxes of a stage are issued by several lanes at once
   // (lane j its j-th box) after lane 0 has armed the stage's full barrier
   // with its bytes; every box is read once, so it enters L2 with the
-  // evict-first policy.  The first stages go out before the block-wide
-  // barrier below, the rest after each stage is released.
+  // evict-first policy.  The first kStages stages go out at once, every later
+  // one as soon as the consumers have released its slot.
   const uint32_t box_bytes = box_t * D * 2;  // one piece: box_t rows, all D dims
   const int per_piece = box_t < kTile ? 1 : D / 64;
   const int nbox = pieces_per_tile * per_piece * 2;

@@ -121,3 +121,39 @@ def test_cluster_bad_rows_are_zero(pkg):
     ref = oracle.decode_attn(w2.q.cpu(), w2.k_pages.cpu(), w2.v_pages.cpu(), table.cpu(),
                              seq.cpu(), w.scale, 0, rows=np.r_[0:8, 40:48])
     check(out.view(-1, 128)[np.r_[0:8, 40:48]], ref, torch.float16)
+
+
+def test_cluster_stall_with_empty_shards_reports_timeout_and_recovers(pkg):
+    """A cluster plan whose clusters hold empty shards (a 300-token and an
+    empty sequence beside a 9000-token one), with every CTA's first-stage
+    barrier made to expect 64 bytes more than its copies bring (the library's
+    DECODE_ATTN_TEST_STALL_TX hook): the empty shards reach the exchange at
+    once and must still wait for their partners, whose consumers give up
+    after about 2 s.  The call ends by itself with DECODE_ATTN_DEV_TIMEOUT and
+    zero rows; the next call is again bit-identical to the workspace merge and
+    within tolerance of the oracle."""
+    import os
+    lens = [9000, 300, 0, 4097]
+    w = workloads.make_custom("cs", batch=4, num_q_heads=64, num_kv_heads=8, head_dim=128,
+                              page_size=64, seq_lens=[max(L, 1) for L in lens], seed=87,
+                              decoy_pages=3)
+    L = torch.tensor(lens, dtype=torch.int32)
+    ref = oracle.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, L, w.scale, 0)
+    wd, Ld = w.to(DEV), L.to(DEV)
+    params = pkg.make_params(wd.q, wd.k_pages, wd.page_table, w.scale, 0, 9000, 0, 0, 0,
+                             CLUSTER)
+    plan = pkg.decode_attn_make_plan(params,
+                                     torch.cuda.get_device_properties(DEV).multi_processor_count)
+    assert plan.cluster == plan.max_shards >= 2, plan.as_dict()
+    os.environ["DECODE_ATTN_TEST_STALL_TX"] = "64"
+    try:
+        out, err = run(pkg, wd.q, wd, Ld, 0, 9000, CLUSTER)
+    finally:
+        del os.environ["DECODE_ATTN_TEST_STALL_TX"]
+    assert err & pkg.DEV_TIMEOUT
+    assert torch.all(out == 0)
+    out_c, err_c = run(pkg, wd.q, wd, Ld, 0, 9000, CLUSTER)
+    out_g, err_g = run(pkg, wd.q, wd, Ld, 0, 9000, GRID)
+    assert err_c == 0 and err_g == 0
+    assert torch.equal(out_c, out_g)
+    check(out_c, ref, torch.float16)
