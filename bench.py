@@ -220,16 +220,20 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the split kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    summary, if it was taken of the same kernel on the current kernel
+    sources (the summaries are captured with the default options: fp16, one
+    query position, no append; the caller passes None for other runs)."""
     path = os.path.join(ROOT, "profiles", f"split_kernel_{workload}.md")
-    if not os.path.exists(path):
+    if kernel is None or not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    kn = re.search(r"^kernel:\s*(\S+)", text, re.M)
     hsh = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
-    if not m or not hsh or hsh.group(1) != kernel_source_hash():
+    if not m or not kn or kn.group(1) != kernel or not hsh or \
+            hsh.group(1) != kernel_source_hash():
         return None
     return float(m.group(1))
 
@@ -564,7 +568,9 @@ def gpu_arm(args):
     value_tbs = bytes_all / (ms_max * 1e-3) / 1e12
     peak_gbs, peak_src = load_peak_hbm()
     split_achieved_gbs = kv_bytes / (split_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    default_run = T == 1 and not args.append and args.dtype == "fp16"
+    traffic = recorded_traffic(args.workload,
+                               split_kernel_name(plan, w.head_dim) if default_run else None)
     # ---- every other configuration of the benchmark, timed the same way
     per_config = None
     if rank == 0 and args.config_steps > 0 and T == 1 and not args.append and \

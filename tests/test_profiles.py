@@ -48,3 +48,21 @@ def test_summaries_share_one_kernel_source():
     for name in os.listdir(os.path.join(ROOT, "profiles")):
         hashes.update(re.findall(r"kernel_source_sha256[`:\s]+([0-9a-f]{16})", read(name)))
     assert len(hashes) == 1, hashes
+
+
+@pytest.mark.parametrize("workload", sorted(ALGORITHMIC))
+def test_traffic_applies_only_to_the_captured_kernel(workload):
+    """bench.py reports a summary's traffic only for runs of the kernel the
+    summary captured (and only with the default options, for which the
+    caller passes that kernel's name)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    kernel = re.search(r"^kernel:\s*(\S+)$", read(f"split_kernel_{workload}.md"), re.M)
+    assert kernel and kernel.group(1).startswith("split_")
+    assert bench.recorded_traffic(workload, "split_simt_kernel_other") is None
+    assert bench.recorded_traffic(workload, None) is None
+    got = bench.recorded_traffic(workload, kernel.group(1))
+    if got is not None:  # the summary was taken on the current kernel sources
+        m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", read(f"split_kernel_{workload}.md"))
+        assert got == float(m.group(1))
