@@ -645,6 +645,10 @@ def gpu_arm(args):
                          "achieved": split_achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": split_achieved_gbs / peak_gbs, "peak_source": peak_src,
                          "traffic": traffic,
+                         # every byte the launch moves (ncu DRAM read + write:
+                         # K/V, q, page table, partials, out) over its time
+                         "traffic_gbs": (traffic / (split_avg_ms * 1e-3) / 1e9
+                                         if traffic else None),
                          "algorithmic_bytes_per_launch": kv_bytes,
                          "launch_us": split_avg_ms * 1e3,
                          "launch_us_percentiles": percentiles_us(split_ms)},

@@ -45,6 +45,10 @@ def test_bench_line_and_dump_match_the_oracle(gpu, tmp_path, name):
     roof = line["roofline"]
     assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    if roof["traffic"] is None:
+        assert roof["traffic_gbs"] is None
+    else:
+        assert abs(roof["traffic_gbs"] - roof["traffic"] / roof["launch_us"] / 1e3) < 1e-6
     for pc in (roof["launch_us_percentiles"], line["step_us_percentiles"]):
         assert 0 < pc["p10"] <= pc["p50"] <= pc["p90"]
     if name == "tiny":
