@@ -145,8 +145,9 @@ size_t simt_smem_bytes(int head_dim) {
 // over chunks of kMinChunk..max_chunk tokens, at most `slots` CTAs and at
 // least two shards (the length is above the split threshold); ties go to
 // more CTAs.  Against the chunk sweeps it picks the measured best or a
-// plan within 1 % of it (one 131072-token sequence: 24 shards, 91.1 us, where
-// 1.7 waves took 102.7 us; the Llama shape: 16 shards, 16.5 against 18.5 us).
+// plan within 1 % of it (one 131072-token sequence: 32 shards, 89.1 us,
+// against 92.0 at 24 and 94.3 at 38; the Llama shape: 16 shards, 14.3-14.4
+// us, against 14.5-15.2 at 12 and 15.3 at 24).
 int64_t one_wave_shards(int64_t units, int64_t slots, int64_t span, int head_dim,
                         int64_t max_chunk) {
   const int stages = head_dim == 64 ? 6 : 3;
@@ -497,8 +498,6 @@ int run_split(const decode_attn_params* p, const decode_attn_plan& plan, const v
                plan.ring_stages == (p->head_dim == 64 ? 4 : 2))
                   ? 1
                   : 0;  // the launcher has the shallow kernels the planner picks from
-  L.batch = p->batch;
-  L.num_sms = plan.ctas_per_sm > 0 ? plan.grid_x / plan.ctas_per_sm : plan.grid_x;
   L.stream = stream;
   // the shard tickets are zero on entry: the last CTA of each group clears
   // its own, so a workspace cleared once stays clear across calls

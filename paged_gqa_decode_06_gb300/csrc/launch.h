@@ -21,8 +21,6 @@ struct SplitLaunch {
   int dtype;
   int shallow;      // tensor-core kernel with the shallow ring (MmaCfg kShallow)
   int cluster;      // > 0: the cluster-merge kernel, clusters of this many CTAs along x
-  int batch;
-  int num_sms;
   cudaStream_t stream;
 };
 
