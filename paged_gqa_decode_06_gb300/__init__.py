@@ -4,7 +4,7 @@ Thin binding over the C ABI in ``include/decode_attn.h`` (the shared library
 ``_build/libpaged_gqa_decode.so``, built by ``build.build()``).  This module
 only marshals arguments: torch tensors become raw device pointers, the
 current CUDA stream becomes the ``stream`` argument, and the workspace is a
-torch allocation cached per device.  Every step of the computation runs in
+torch allocation cached per device and stream.  Every step of the computation runs in
 the library's CUDA kernels; there is no other code path, and calling any
 entry point without the built library raises.
 
@@ -185,16 +185,24 @@ def decode_attn_workspace_clear(params: DecodeAttnParams, workspace, stream=None
 _ws_cache: dict = {}
 
 
-def _workspace(device, nbytes: int):
+def _workspace(device, nbytes: int, stream=None):
+    """The cached workspace of (device, stream): calls on different streams
+    may run at the same time, so each stream has its own tickets and
+    partials.  A buffer is allocated zero-filled on the stream it serves, so
+    the fill is ordered before that stream's kernels (and a replaced buffer
+    is only reused by later work of the same stream)."""
     import torch
     if nbytes == 0:
         return None
-    key = (device.index if device.index is not None else torch.cuda.current_device())
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(index)
+    key = (index, s.cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         # zero-filled: its shard tickets must start at zero (the kernels leave
         # them zero after every completed call)
-        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        with torch.cuda.stream(s):
+            buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
 
@@ -222,7 +230,7 @@ def _stream_handle(stream) -> int:
 
 
 def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_seq_len,
-             variant, split_min, force_chunk, workspace, schedule=SCHEDULE_AUTO):
+             variant, split_min, force_chunk, workspace, schedule=SCHEDULE_AUTO, stream=None):
     import torch
     dev = q.device
     if dev.type != "cuda":
@@ -244,7 +252,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
     need = decode_attn_workspace_size(p, dev.index if dev.index is not None else
                                       torch.cuda.current_device())
     if workspace is None:
-        workspace = _workspace(dev, need)
+        workspace = _workspace(dev, need, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return p, out, workspace, ws_bytes
 
@@ -259,10 +267,12 @@ def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window:
     int32, seq_lens [B] int32, all on one CUDA device.  ``window`` > 0 attends
     the last min(L, window) positions.  ``err_flag``: optional int32 device
     tensor of one element that receives DEV_* bits.  Enqueued on ``stream``
-    (default: torch's current stream); does not synchronise."""
+    (default: torch's current stream); does not synchronise.  ``workspace``:
+    by default a zero-filled buffer cached per (device, stream); pass one to
+    keep its fill out of a captured graph."""
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace, schedule)
+                                    workspace, schedule, stream)
     st = load_library().decode_attn(ctypes.byref(p), _ptr(q), _ptr(k_pages), _ptr(v_pages),
                                     _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(ws),
                                     ws_bytes, _ptr(err_flag), _stream_handle(stream))
@@ -311,7 +321,7 @@ def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, 
     import torch
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace, schedule)
+                                    workspace, schedule, stream)
     _check(k_new, q.dtype, "k_new", q.device)
     _check(v_new, q.dtype, "v_new", q.device)
     st = load_library().decode_attn_append(ctypes.byref(p), _ptr(q), _ptr(k_new), _ptr(v_new),
@@ -331,7 +341,7 @@ def decode_attn_split(q, k_pages, v_pages, page_table, seq_lens, scale: float, w
     partials into ``workspace`` otherwise).  Returns (out, workspace)."""
     p, out, ws, ws_bytes = _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale,
                                     window, max_seq_len, variant, split_min, force_chunk,
-                                    workspace, schedule)
+                                    workspace, schedule, stream)
     st = load_library().decode_attn_split(ctypes.byref(p), _ptr(q), _ptr(k_pages),
                                           _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
                                           _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),

@@ -379,9 +379,9 @@ def test_variants_agree(pkg, name):
 
 @pytest.mark.parametrize("name", ["llama", "long_w4096", "tiny"])
 def test_cuda_graph_capture_of_a_step(pkg, name):
-    """A decode step captured once as a CUDA graph (split kernel, then the
-    combine as a programmatic dependent launch) replays to the same bits as
-    the eager call, also after the inputs change in place."""
+    """A decode step captured once as a CUDA graph (one launch: the split
+    kernel, whose last CTA per group or whose cluster merges) replays to the
+    same bits as the eager call, also after the inputs change in place."""
     w = workloads.make(name, device=DEV)
     ref, _ = run(pkg, w)
     out = torch.empty_like(w.q)
@@ -499,3 +499,25 @@ def test_stalled_pipeline_reports_timeout_and_recovers(pkg):
     out, err = run(pkg, w, workspace=ws)
     assert err == 0
     assert_parity(out, oracle_of(w))
+
+
+def test_streams_get_their_own_workspace(pkg):
+    """Calls on two streams at once use two cached workspaces (their shard
+    tickets and partials would otherwise race), each zero-filled on its own
+    stream; both give the single-stream bits."""
+    w = workloads.make("llama", device=DEV)
+    ref, _ = run(pkg, w)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    torch.cuda.synchronize()
+    for s in (s1, s2):
+        with torch.cuda.stream(s):
+            outs.append(pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
+                                        w.scale, max_seq_len=w.max_seq_len()))
+    torch.cuda.synchronize()
+    keys = {k for k in pkg._ws_cache if k[1] in (s1.cuda_stream, s2.cuda_stream)}
+    assert len(keys) == 2
+    a, b = (pkg._ws_cache[k] for k in keys)
+    assert a.data_ptr() != b.data_ptr()
+    for out in outs:
+        assert torch.equal(out, ref)
