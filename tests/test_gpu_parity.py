@@ -122,6 +122,21 @@ def test_parity_long(pkg, name, variant):
     assert_parity(out, oracle_of(w), what=name)
 
 
+@pytest.mark.parametrize("name", ["long_b1", "long_d256", "seq65536x2", "many_short"])
+def test_parity_measured_shapes(pkg, name):
+    """The other shapes the measurements quote, at full size and with the
+    planner's plans (32 near-equal shards merged through the workspace; the
+    head_dim-256 form at one CTA per SM; two sequences of 65536; a thousand
+    short sequences on the shallow ring): every row against the oracle, and
+    the same bits on a second run."""
+    w = workloads.make(name, device=DEV)
+    out, err = run(pkg, w)
+    assert err == 0
+    assert_parity(out, oracle_of(w), what=name)
+    again, err = run(pkg, w)
+    assert err == 0 and torch.equal(out, again)
+
+
 # ------------------------------------------------------- bit-exact facts
 
 def small_pool(rng_seed, B, Hq, Hkv, D, PS, lens, decoys=4):
