@@ -101,13 +101,67 @@ __device__ __forceinline__ void merge_batch(const CombineArgs& a, int g, int qua
 // bytes, 16-byte aligned; up to `cap` (m, l) pairs per row are staged there,
 // more are read from global memory).  `sync` is a barrier over exactly those
 // threads; slot_of(r, s) locates the partial of row r, shard s.  dead forces
-// zero rows (an invalid range).
-template <int D, class E, class Sync, class SlotOf>
+// zero rows (an invalid range).  kOneTrip > 0: a group of at most kOneTrip
+// shards with one output item per thread skips the staging and loads
+// everything at once (below); the bits are the same either way.
+template <int D, class E, int kOneTrip = 0, class Sync, class SlotOf>
 __device__ __forceinline__ void merge_group(const CombineArgs& a, int b, int h, int S, bool dead,
                                             int tid, int nthreads, uint8_t* smem, int cap,
                                             Sync sync, SlotOf slot_of) {
   constexpr int kQuads = D / 4;
   const int G = a.T * a.G;  // rows of the group
+  if constexpr (kOneTrip > 0) if (G * kQuads <= nthreads && S >= 1 && S <= kOneTrip) {
+    // One L2 round trip for groups of at most kOneTrip shards and one item
+    // per thread: every (m, l) and accumulator of the item is loaded at once
+    // (shard indices clamped to the group's last, so no load sits behind a
+    // branch), the row's maximum is taken in registers, then the same
+    // multiply-adds in the same shard order as below: the same bits.
+    const int e = tid;
+    if (e >= G * kQuads) return;
+    const int g = e / kQuads, quad = e % kQuads;
+    float4 x[kOneTrip];
+    float2 v[kOneTrip];
+#pragma unroll
+    for (int u = 0; u < kOneTrip; ++u) {
+      const size_t slot = slot_of(g, min(u, S - 1));
+      const bool in = PGD_IN(slot, slot_bound(a), a.err);
+      x[u] = in ? __ldcg(reinterpret_cast<const float4*>(a.ws_acc + slot * D) + quad)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = in ? __ldcg(a.ws_ml + slot) : make_float2(-INFINITY, 0.f);
+    }
+    float M = -INFINITY;
+    bool zero = dead;
+#pragma unroll
+    for (int u = 0; u < kOneTrip; ++u)
+      if (u < S) {
+        zero |= v[u].y < 0.f;  // a shard saw a bad page or gave up waiting
+        M = fmaxf(M, v[u].x);
+      }
+    zero |= M == -INFINITY;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+#pragma unroll
+    for (int u = 0; u < kOneTrip; ++u)
+      if (!zero && u < S) {
+        const float c = fast_exp2(v[u].x - M);
+        L = __fmaf_rn(c, v[u].y, L);
+        o.x = __fmaf_rn(c, x[u].x, o.x);
+        o.y = __fmaf_rn(c, x[u].y, o.y);
+        o.z = __fmaf_rn(c, x[u].z, o.z);
+        o.w = __fmaf_rn(c, x[u].w, o.w);
+      }
+    const bool z = zero || L == 0.f;
+    const uint32_t lo = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.x, L), z ? 0.f : __fdiv_rn(o.y, L));
+    const uint32_t hi = ElemOps<E>::pack2(z ? 0.f : __fdiv_rn(o.z, L), z ? 0.f : __fdiv_rn(o.w, L));
+    const size_t row = group_row(b, h, g, a.T, a.G, a.Hq);
+    if (PGD_IN(row, (size_t)a.B * a.T * a.Hq, a.err)) {
+      uint32_t* dst =
+          reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + row * D + 4 * quad);
+      dst[0] = lo;
+      dst[1] = hi;
+    }
+    return;
+  }
   float2* ml_s = reinterpret_cast<float2*>(smem);                // [G][cap]
   float* max_s = reinterpret_cast<float*>(smem + G * cap * 8);   // [G]
   int* zero_s = reinterpret_cast<int*>(max_s + kMaxMergeRows);   // [G]

@@ -377,8 +377,9 @@ __device__ __forceinline__ void cluster_finish(const SplitArgs& a, const Cluster
 // cluster per (KV head, sequence), one CTA per shard, cluster rank = shard),
 // merged through distributed shared memory (ClusterXchg, cluster_finish);
 // other split plans write their partial to the workspace and the group's last
-// CTA merges (merge_if_last).
-template <int D, int NT8, class E, bool SH, bool CL = false>
+// CTA merges (merge_if_last; kOneTrip > 0: groups of at most that many shards
+// in one L2 round trip, merge_group).
+template <int D, int NT8, class E, bool SH, bool CL = false, int kOneTrip = 0>
 __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
                                                const CUtensorMap& tmap_v, const SplitArgs& a) {
   using C = MmaCfg<D, SH>;
@@ -752,17 +753,30 @@ __device__ __forceinline__ void split_mma_body(const CUtensorMap& tmap_k,
   if constexpr (CL) {
     cluster_finish<D, E>(a, x, b, h, smem_u32(&recv_bar), recv, kWarps * 32);
   } else {
-    merge_if_last<D, E>(a, r, b, h, ring, kWarps * 32);
+    merge_if_last<D, E, kOneTrip>(a, r, b, h, ring, kWarps * 32);
   }
 }
 
-// The split kernel with the deep ring.  Its launch bounds name no CTA count:
-// the register allocation it gets that way leaves two CTAs per SM at
-// D <= 128.
+// The split kernel with the deep ring, for split plans: the last CTA of a
+// group of up to 16 shards merges them in one L2 round trip.  Its launch
+// bounds name no CTA count: the register allocation it gets that way leaves
+// two CTAs per SM at D <= 128.
 template <int D, int NT8, class E>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads)
     split_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
+  split_mma_body<D, NT8, E, false, false, 16>(tmap_k, tmap_v, a);
+}
+
+// The deep-ring kernel of single-pass plans: the same body without the
+// one-round-trip merge (a single-pass plan never merges).  Kept apart
+// because the short single-CTA steps are sensitive to the code they run:
+// with the merge form compiled in, or with the merge code compiled out,
+// they measured 0.5-0.8 us slower on GB300.
+template <int D, int NT8, class E>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads)
+    split_mma_kernel_single(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const SplitArgs a) {
   split_mma_body<D, NT8, E, false>(tmap_k, tmap_v, a);
 }
 

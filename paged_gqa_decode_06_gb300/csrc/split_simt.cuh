@@ -156,7 +156,8 @@ __device__ __forceinline__ void append_new_rows(const SplitArgs& a, const SeqRan
 // barrier orders the other threads' writes before it), and in the last CTA
 // its acquire, passed on by the next barrier, makes every other CTA's
 // partial visible to the merge.
-template <int D, class E = __half>
+// kOneTrip: as merge_group's (0: the staged form for every group).
+template <int D, class E = __half, int kOneTrip = 0>
 __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange& r, int b, int h,
                                               uint8_t* smem, int nthreads) {
   __shared__ int is_last_s;
@@ -187,9 +188,9 @@ __device__ __forceinline__ void merge_if_last(const SplitArgs& a, const SeqRange
   c.chunk = a.chunk;
   c.balanced = a.balanced;
   c.max_shards = a.max_shards;
-  merge_group<D, E>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem, kShardBlock,
-                    [nthreads] { named_barrier_sync(1, nthreads); },
-                    GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});
+  merge_group<D, E, kOneTrip>(c, b, h, r.nshards, false, threadIdx.x, nthreads, smem,
+                              kShardBlock, [nthreads] { named_barrier_sync(1, nthreads); },
+                              GridSlots{b, h, a.T, a.G, a.Hq, a.max_shards});
   if (threadIdx.x == 0) *ticket = 0;
 }
 
