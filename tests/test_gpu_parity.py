@@ -137,6 +137,37 @@ def test_parity_measured_shapes(pkg, name):
     assert err == 0 and torch.equal(out, again)
 
 
+@pytest.mark.parametrize("shards", [2, 3, 8, 15, 16, 17, 24])
+def test_merge_forms_agree_across_the_shard_boundary(pkg, shards):
+    """The fused merge takes its one-round-trip form for groups of at most
+    16 shards (one output item per thread) and the staged form above; the
+    standalone combine always stages.  Forced chunks give every group of a
+    G = 4, D = 128 shape exactly `shards` shards (the shorter sequences fewer,
+    down to one): the fused result must equal the standalone combine's bit
+    for bit and the oracle within tolerance."""
+    chunk = 64
+    L = shards * chunk
+    lens = [L, max(1, L - 100), (L + 1) // 2]
+    w = workloads.make_custom("m", batch=3, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                              page_size=16, seq_lens=lens, seed=500 + shards, device=DEV)
+    kw = dict(max_seq_len=L, force_chunk=chunk, schedule=1)
+    params = pkg.make_params(w.q, w.k_pages, w.page_table, w.scale, 0, L, 0, 0, chunk, 1)
+    plan = pkg.decode_attn_make_plan(params,
+                                     torch.cuda.get_device_properties(DEV).multi_processor_count)
+    assert plan.max_shards == shards and plan.cluster == 0, plan.as_dict()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, ws = pkg.decode_attn_split(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens,
+                                    w.scale, err_flag=err, **kw)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    fused = out.clone()
+    out.zero_()
+    pkg.decode_attn_combine(params, w.seq_lens, out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(fused, out)
+    assert_parity(fused, oracle_of(w), what=shards)
+
+
 # ------------------------------------------------------- bit-exact facts
 
 def small_pool(rng_seed, B, Hq, Hkv, D, PS, lens, decoys=4):
