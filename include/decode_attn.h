@@ -103,7 +103,9 @@ typedef struct decode_attn_params {
   float scale;               /* multiplies q . k before the softmax */
   int32_t window;            /* <= 0: whole context; else the last min(L, window) positions */
   int32_t variant;           /* DECODE_ATTN_VARIANT_*; 0 = automatic */
-  int32_t split_min;         /* contexts above this use shards + combine; <= 0 means 256 */
+  int32_t split_min;         /* contexts above this use shards + combine; <= 0 means 256;
+                                a context longer than one shard holds (1024 boxes of
+                                min(page_size, 64) positions) is split regardless */
   int32_t force_chunk;       /* > 0: tokens per shard (rounded up to 64); 0 = planner */
   int32_t num_queries;       /* T new query positions per sequence (<= 0 means 1); with
                                 T > 1, q and out are [B][T][Hq][D], query t of sequence b

@@ -236,7 +236,9 @@ extern "C" int decode_attn_make_plan(const decode_attn_params* p, int32_t num_sm
     chunk = round_up(force_chunk, kTile);
     if (chunk > max_chunk) return DECODE_ATTN_ERR_SHAPE;
   } else if (attended <= split_min) {
-    chunk = round_up(span, kTile);  // one shard covers the whole range
+    // one shard covers the whole range, unless the range is longer than one
+    // shard can hold (kMaxPieces boxes): then the fewest shards that fit
+    chunk = std::min(round_up(span, kTile), max_chunk);
   } else {
     // Shard count from the work bound (every (sequence, KV head) unit at the
     // longest length) and the CTA slots (SMs x resident CTAs), calibrated on

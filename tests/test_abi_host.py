@@ -123,6 +123,20 @@ def test_threshold_at_256(pkg):
     assert plan.split == 0
 
 
+@pytest.mark.parametrize("page_size,length,shards", [(8, 9000, 2), (8, 8192, 1),
+                                                     (16, 40000, 3), (64, 9000, 1)])
+def test_single_pass_request_longer_than_one_shard_splits(pkg, page_size, length, shards):
+    """A split threshold above the context asks for one shard, but a shard
+    holds at most 1024 TMA boxes of min(page, 64) positions: a longer range
+    is cut into the fewest shards that fit instead of being refused."""
+    p = params(pkg, page_size=page_size, max_pages_per_seq=(length + page_size - 1) // page_size,
+               num_pages=4096, max_seq_len=length, split_min=100000)
+    plan = pkg.decode_attn_make_plan(p, 152)
+    box = min(page_size, 64)
+    assert plan.max_shards == shards and plan.split == (shards > 1)
+    assert plan.chunk_tokens <= 1024 * box and plan.chunk_tokens % 64 == 0
+
+
 def test_few_units_take_one_wave(pkg):
     # B=4, Hkv=8, 131072 tokens, D=128: 32 (b, h) units on 152 SMs x 2 CTAs.
     # Fewer units than slots: one wave, shard count from the cost model

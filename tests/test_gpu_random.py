@@ -51,7 +51,10 @@ def draw(seed):
                 force_chunk=force_chunk, lmax=lmax)
 
 
-@pytest.mark.parametrize("seed", range(40))
+# seeds 0..39, plus three drawn from a wider sweep that ask for a single
+# pass over more positions than one shard holds (pages of 8, split_min
+# 100000, contexts near 9000)
+@pytest.mark.parametrize("seed", list(range(40)) + [98, 204, 419])
 def test_random_configuration_matches_oracle(pkg, seed):
     c = draw(seed)
     Hq = c["Hkv"] * c["G"]
