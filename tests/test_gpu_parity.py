@@ -168,6 +168,37 @@ def test_merge_forms_agree_across_the_shard_boundary(pkg, shards):
     assert_parity(fused, oracle_of(w), what=shards)
 
 
+MAX_CASES = {
+    # one sequence of 2^20 positions (4 GiB of K+V; 32 shards of 32768)
+    "ctx1M": (dict(batch=1, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
+                   seq_lens=[1 << 20]), 0),
+    # the same with a 4096-position window
+    "ctx1M_window": (dict(batch=1, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
+                          seq_lens=[1 << 20]), 4096),
+    # 2^21 positions in pages of 16 at D = 64: 128 shards of 16384, the staged merge
+    "ctx2M_d64": (dict(batch=1, num_q_heads=16, num_kv_heads=4, head_dim=64, page_size=16,
+                       seq_lens=[2 << 20]), 0),
+    # 8192 sequences of 1..128 positions: a grid 8192 deep, single pass
+    "b8192": (dict(batch=8192, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                   seq_lens=[int(x) for x in np.random.default_rng(5).integers(1, 129, 8192)]), 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MAX_CASES))
+def test_parity_at_large_sizes(pkg, name):
+    """Long contexts and deep grids, every row against the oracle, the same
+    bits on a second run."""
+    kw, window = MAX_CASES[name]
+    w = workloads.make_custom(name, seed=13, device=DEV, **kw)
+    L = max(kw["seq_lens"])
+    out, err = run(pkg, w, window=window, max_seq_len=L)
+    assert err == 0
+    again, _ = run(pkg, w, window=window, max_seq_len=L)
+    assert torch.equal(out, again)
+    assert_parity(out, oracle_of(w, window=window), what=name)
+    del w
+
+
 # ------------------------------------------------------- bit-exact facts
 
 def small_pool(rng_seed, B, Hq, Hkv, D, PS, lens, decoys=4):
