@@ -248,6 +248,8 @@ def split_kernel_name(plan, head_dim: int) -> str:
         return "split_mma_kernel_cluster"
     if plan.ring_stages == (4 if head_dim == 64 else 2):
         return "split_mma_kernel_shallow"
+    if not plan.split:
+        return "split_mma_kernel_single"
     return "split_mma_kernel"
 
 

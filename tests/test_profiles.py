@@ -66,3 +66,22 @@ def test_traffic_applies_only_to_the_captured_kernel(workload):
     if got is not None:  # the summary was taken on the current kernel sources
         m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", read(f"split_kernel_{workload}.md"))
         assert got == float(m.group(1))
+
+
+def test_kernel_names_follow_the_plan():
+    """The kernel bench.py names for a plan: the one the launcher picks
+    (cluster, shallow ring, single pass, or the split kernel)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from types import SimpleNamespace as P
+    assert bench.split_kernel_name(P(variant=2, cluster=8, ring_stages=3, split=1), 128) == \
+        "split_mma_kernel_cluster"
+    assert bench.split_kernel_name(P(variant=2, cluster=0, ring_stages=2, split=0), 128) == \
+        "split_mma_kernel_shallow"
+    assert bench.split_kernel_name(P(variant=2, cluster=0, ring_stages=3, split=0), 128) == \
+        "split_mma_kernel_single"
+    assert bench.split_kernel_name(P(variant=2, cluster=0, ring_stages=6, split=1), 64) == \
+        "split_mma_kernel"
+    assert bench.split_kernel_name(P(variant=1, cluster=0, ring_stages=3, split=1), 128) == \
+        "split_simt_kernel"
