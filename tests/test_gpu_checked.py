@@ -15,7 +15,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gpu_parity.py", "tests/test_gpu_append.py", "tests/test_gpu_multi.py",
           "tests/test_gpu_bf16.py", "tests/test_gpu_cluster.py", "tests/test_gpu_poison.py",
-          "tests/test_gpu_invariants.py"]
+          "tests/test_gpu_invariants.py", "tests/test_gpu_random.py",
+          "tests/test_gpu_properties_random.py"]
 
 
 def test_gpu_suites_pass_on_the_checked_build():
