@@ -15,6 +15,7 @@ Entry points (same names as the C ABI):
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 from typing import Optional
@@ -115,6 +116,25 @@ def load_library():
     return _lib
 
 
+def _on_device_of(name: str, index: int):
+    """Runs the wrapped call with the CUDA device of its tensor argument
+    `name` (positional `index`) current: the library launches on the current
+    device, and the default stream is that device's current stream, so
+    tensors on another GPU than the current one still get their own device."""
+    def deco(fn):
+        @functools.wraps(fn)
+        def wrapper(*args, **kwargs):
+            import torch
+            t = kwargs.get(name, args[index] if len(args) > index else None)
+            if isinstance(t, torch.Tensor) and t.is_cuda and \
+                    t.device.index not in (None, torch.cuda.current_device()):
+                with torch.cuda.device(t.device):
+                    return fn(*args, **kwargs)
+            return fn(*args, **kwargs)
+        return wrapper
+    return deco
+
+
 def decode_attn_strerror(code: int) -> str:
     return load_library().decode_attn_strerror(int(code)).decode()
 
@@ -170,6 +190,7 @@ def decode_attn_workspace_size(params: DecodeAttnParams, device: int) -> int:
     return int(load_library().decode_attn_workspace_size(ctypes.byref(params), int(device)))
 
 
+@_on_device_of("workspace", 1)
 def decode_attn_workspace_clear(params: DecodeAttnParams, workspace, stream=None) -> None:
     """Zeroes the workspace's shard tickets (needed once for a workspace that
     was not allocated zero-filled, or after a DEV_TIMEOUT / DEV_WORKSPACE)."""
@@ -224,9 +245,15 @@ def _check(t, dtype, name, device=None):
 
 
 def _stream_handle(stream) -> int:
+    """The raw handle of `stream`, by default the current device's current
+    stream; a stream of another device than the current one is refused."""
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {stream.device}, the tensors on "
+                         f"cuda:{torch.cuda.current_device()}")
+    return stream.cuda_stream
 
 
 def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_seq_len,
@@ -257,6 +284,7 @@ def _prepare(q, k_pages, v_pages, page_table, seq_lens, out, scale, window, max_
     return p, out, workspace, ws_bytes
 
 
+@_on_device_of("q", 0)
 def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
                 out=None, max_seq_len: Optional[int] = None, workspace=None, err_flag=None,
                 variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
@@ -281,6 +309,7 @@ def decode_attn(q, k_pages, v_pages, page_table, seq_lens, scale: float, window:
     return out
 
 
+@_on_device_of("k_pages", 3)
 def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_flag=None,
                      stream=None):
     """Writes the step's new rows k_new/v_new [B,Hkv,D] at positions[b]
@@ -310,6 +339,7 @@ def decode_kv_append(k_new, v_new, positions, k_pages, v_pages, page_table, err_
         raise DecodeAttnError(st, "decode_kv_append")
 
 
+@_on_device_of("q", 0)
 def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, scale: float,
                        window: int = 0, out=None, max_seq_len: Optional[int] = None,
                        workspace=None, err_flag=None, variant: int = VARIANT_AUTO,
@@ -333,6 +363,7 @@ def decode_attn_append(q, k_new, v_new, k_pages, v_pages, page_table, seq_lens, 
     return out
 
 
+@_on_device_of("q", 0)
 def decode_attn_split(q, k_pages, v_pages, page_table, seq_lens, scale: float, window: int = 0,
                       out=None, max_seq_len=None, workspace=None, err_flag=None,
                       variant: int = VARIANT_AUTO, split_min: int = 0, force_chunk: int = 0,
@@ -351,6 +382,7 @@ def decode_attn_split(q, k_pages, v_pages, page_table, seq_lens, scale: float, w
     return out, ws
 
 
+@_on_device_of("out", 2)
 def decode_attn_combine(params: DecodeAttnParams, seq_lens, out, workspace, err_flag=None,
                         stream=None):
     """The ordered combine alone, for ``params`` as used by decode_attn_split."""
@@ -363,6 +395,7 @@ def decode_attn_combine(params: DecodeAttnParams, seq_lens, out, workspace, err_
     return out
 
 
+@_on_device_of("d_q", 7)
 def decode_attn_host(params: DecodeAttnParams, q_host, k_host, v_host, table_host, lens_host,
                      out_host, d_q, d_k, d_v, d_table, d_lens, d_out, workspace,
                      kv_bytes_to_copy: int = 0, err_flag=None, stream=None):
@@ -390,6 +423,7 @@ def _static_scratch_fn():
     return f
 
 
+@_on_device_of("q", 0)
 def decode_attn_static_scratch(q, k_pages, v_pages, page_table, seq_lens, scale: float,
                                window: int = 0, out=None, max_seq_len: Optional[int] = None,
                                err_flag=None, variant: int = VARIANT_AUTO, split_min: int = 0,

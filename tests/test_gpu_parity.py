@@ -598,3 +598,29 @@ def test_streams_get_their_own_workspace(pkg):
     assert a.data_ptr() != b.data_ptr()
     for out in outs:
         assert torch.equal(out, ref)
+
+
+def test_calls_run_on_the_tensors_device(pkg):
+    """The binding makes the tensors' device current for the call (the
+    library launches on the current device) and takes that device's current
+    stream by default; an explicit stream of that device gives the same bits.
+    With a second GPU, tensors there are served while cuda:0 is current."""
+    w = workloads.make("llama", device=DEV)
+    ref, _ = run(pkg, w)
+    s = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()
+    out = pkg.decode_attn(w.q, w.k_pages, w.v_pages, w.page_table, w.seq_lens, w.scale,
+                          max_seq_len=w.max_seq_len(), stream=s)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    if torch.cuda.device_count() < 2:
+        return
+    w1 = w.to("cuda:1")
+    with torch.cuda.device(0):
+        out1 = pkg.decode_attn(w1.q, w1.k_pages, w1.v_pages, w1.page_table, w1.seq_lens,
+                               w1.scale, max_seq_len=w.max_seq_len())
+        with pytest.raises(ValueError):
+            pkg.decode_attn(w1.q, w1.k_pages, w1.v_pages, w1.page_table, w1.seq_lens, w1.scale,
+                            max_seq_len=w.max_seq_len(), stream=torch.cuda.Stream(device=0))
+    torch.cuda.synchronize()
+    assert torch.equal(out1.cpu(), ref.cpu())
