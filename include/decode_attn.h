@@ -29,6 +29,8 @@
  * per-device cache of the SM count).  Entry points are thread-safe.
  * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
  * default stream); nothing synchronises the host.
+ * Device: every call runs on the calling thread's current CUDA device
+ * (cudaGetDevice); the pointers and the stream must belong to it.
  * Errors: a negative return means nothing was launched (bad argument) or a
  * CUDA runtime error was reported while launching; decode_attn_strerror()
  * names it.  Problems only the device can see (a page id outside [0, P) in
